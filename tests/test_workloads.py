@@ -1,0 +1,58 @@
+"""The seeded generator: Philox known-answer vectors, exactness and statistics."""
+import json
+import os
+
+import numpy as np
+
+from continuous_batching_ragged_gb300 import workloads as w
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_philox_known_answers():
+    g = json.load(open(os.path.join(GOLDEN, "philox4x32_10_kat.json")))
+    for vec in g["vectors"]:
+        c = [int(x, 16) for x in vec["counter"]]
+        k = [int(x, 16) for x in vec["key"]]
+        out = w.philox4x32_10(*c, *k)
+        assert [int(x) for x in out] == [int(x, 16) for x in vec["output"]]
+
+
+def test_irwin_hall_moments_and_range():
+    x = w.token_values(123, w.KIND_K, 0, 5, np.arange(2048), range(8), 128, "f32")
+    assert abs(float(x.mean())) < 5e-3
+    assert abs(float(x.std()) - 1.0) < 5e-3
+    assert float(np.abs(x).max()) <= 4.0 * np.sqrt(1.5) + 1e-6
+
+
+def test_bf16_rounding_ties_to_even():
+    # 1 + 2^-8 is halfway between bf16 1.0 and 1.0078125 -> even (1.0)
+    x = np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 0.0], dtype=np.float32)
+    r = w.round_to_bf16(x)
+    assert r.tolist() == [1.0, 1.015625, -2.5, 0.0]
+    import torch
+    t = torch.from_numpy(np.random.default_rng(0).standard_normal(4096).astype(np.float32))
+    assert np.array_equal(w.round_to_bf16(t.numpy()), t.to(torch.bfloat16).float().numpy())
+
+
+def test_values_independent_of_packing():
+    b = w.make_batch([3, 0], [2, 4], num_heads=2, head_dim=8, block_size=4, dtype="bf16", seed=9)
+    q = b.packed(w.KIND_K)
+    h0 = b.history(0, w.KIND_K)
+    h1 = b.history(1, w.KIND_K)
+    assert np.array_equal(q[0:2], h0[3:5])
+    assert np.array_equal(q[2:6], h1[0:4])
+
+
+def test_batch_metadata_shapes():
+    b = w.tiny_fp32()
+    assert b.cu_seqlens_q.tolist() == [0, 4, 5, 6]
+    assert b.context_lens.tolist() == [4, 8, 13]
+    assert b.T == 6
+    sm = b.slot_mapping
+    assert len(set(sm.tolist())) == 6
+    m = w.mixed_step()
+    assert m.T == 2048 and m.num_seqs == 67
+    assert m.q_len[-3:].tolist() == [661, 661, 662] and m.p[-3:].tolist() == [0, 1024, 2048]
+    d = w.decode_step(num_seqs=16)
+    assert np.all((d.p >= 512) & (d.p <= 4096))
