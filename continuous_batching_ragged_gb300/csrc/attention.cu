@@ -1,0 +1,124 @@
+// cb_ragged_attention: argument checks and routing of one packed step.
+//
+// Hugging Face blog "Continuous batching from first principles", section
+// "Continuous batching": decode tokens and prefill chunks share one step;
+// page "continuous-batching", section "Inside the kernel": the attention
+// kernel splits the work by request.  Here a request's rows go to one of two
+// kernels by shape: q_len == 1 (decode) to split-KV on CUDA cores, which is
+// bound by HBM; q_len > 1 (a prefill chunk) to tcgen05 tensor cores, which is
+// a dense contraction.  The two run concurrently on two streams joined by
+// events, so a mixed step costs about the longer of the two, not the sum.
+// fp32 caches take the CUDA-core kernel for every row.
+#include <cmath>
+
+#include "kernels.h"
+#include "runtime.h"
+
+namespace {
+
+bool is_pow2(int32_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+cb_status check_cache(const cb_kv_cache* c, const char* who) {
+  if (!c) return cb::fail(CB_ERR_INVALID, "%s: null cache", who);
+  if (c->num_blocks < 1 || c->block_size < 1 || c->num_heads < 1 || c->head_dim < 1)
+    return cb::fail(CB_ERR_INVALID, "%s: cache dimensions must be >= 1", who);
+  if (c->dtype == CB_DTYPE_BF16) {
+    if (c->head_dim != 128)
+      return cb::fail(CB_ERR_UNSUPPORTED, "%s: bf16 needs head_dim 128", who);
+    if (!is_pow2(c->block_size) || c->block_size < 8 || c->block_size > 128)
+      return cb::fail(CB_ERR_UNSUPPORTED, "%s: bf16 needs block_size in {8,16,32,64,128}", who);
+  } else if (c->dtype == CB_DTYPE_F32) {
+    if (c->head_dim != 64 && c->head_dim != 128)
+      return cb::fail(CB_ERR_UNSUPPORTED, "%s: f32 needs head_dim 64 or 128", who);
+  } else {
+    return cb::fail(CB_ERR_UNSUPPORTED, "%s: unknown dtype", who);
+  }
+  return CB_OK;
+}
+
+}  // namespace
+
+extern "C" size_t cb_attention_workspace_size(const cb_kv_cache* cache, int32_t num_seqs,
+                                              int32_t num_tokens, int32_t max_context_len) {
+  if (!cache || num_seqs < 0 || num_tokens < 0 || max_context_len < 0) return 0;
+  const bool row_mode = cache->dtype == CB_DTYPE_F32;
+  return cb::split_kv_workspace_bytes(row_mode, num_seqs, num_tokens, cache->num_heads,
+                                      cache->head_dim, max_context_len);
+}
+
+extern "C" cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache,
+                                         const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                         const int32_t* block_tables, int32_t num_seqs,
+                                         int32_t num_tokens, int32_t max_blocks_per_seq,
+                                         int32_t max_q_len, int32_t max_context_len, float scale,
+                                         void* out, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+  const char* who = "cb_ragged_attention";
+  cb_status st = check_cache(cache, who);
+  if (st != CB_OK) return st;
+  if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq < 0 || max_q_len < 0 || max_context_len < 0)
+    return cb::fail(CB_ERR_INVALID, "%s: negative size", who);
+  if (num_seqs == 0 || num_tokens == 0) {
+    if (num_seqs != num_tokens && (num_seqs == 0) != (num_tokens == 0))
+      return cb::fail(CB_ERR_INVALID, "%s: num_seqs and num_tokens must both be zero or both positive", who);
+    return CB_OK;
+  }
+  if (num_tokens < num_seqs) return cb::fail(CB_ERR_INVALID, "%s: fewer tokens than sequences", who);
+  if (max_q_len < 1 || max_q_len > num_tokens || max_context_len < max_q_len)
+    return cb::fail(CB_ERR_INVALID, "%s: need 1 <= max_q_len <= num_tokens and max_q_len <= max_context_len", who);
+  if (int64_t(max_blocks_per_seq) * cache->block_size < max_context_len)
+    return cb::fail(CB_ERR_INVALID, "%s: max_blocks_per_seq * block_size < max_context_len", who);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return cb::fail(CB_ERR_INVALID, "%s: scale must be finite and > 0", who);
+  if (!q || !cu_seqlens_q || !context_lens || !block_tables || !out || !cache->k || !cache->v)
+    return cb::fail(CB_ERR_INVALID, "%s: null pointer", who);
+  const uintptr_t align = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
+                          reinterpret_cast<uintptr_t>(cache->k) | reinterpret_cast<uintptr_t>(cache->v);
+  if (align % 16 != 0) return cb::fail(CB_ERR_INVALID, "%s: q, out and the pools must be 16-byte aligned", who);
+
+  unsigned* err = cb::device_error_word();
+  if (!err) return CB_ERR_CUDA;
+  cb::AttnArgs a;
+  a.q = q;
+  a.out = out;
+  a.k_pool = cache->k;
+  a.v_pool = cache->v;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.context_lens = context_lens;
+  a.block_tables = block_tables;
+  a.num_seqs = num_seqs;
+  a.num_tokens = num_tokens;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = cache->num_blocks;
+  a.block_size = cache->block_size;
+  a.num_heads = cache->num_heads;
+  a.head_dim = cache->head_dim;
+  a.max_q_len = max_q_len;
+  a.max_context_len = max_context_len;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.dtype = cache->dtype;
+  a.err = err;
+  cudaStream_t main = static_cast<cudaStream_t>(stream);
+
+  if (cache->dtype == CB_DTYPE_F32) return cb::launch_split_kv(a, true, workspace, workspace_bytes, main);
+
+  if (max_q_len == 1) return cb::launch_split_kv(a, false, workspace, workspace_bytes, main);
+  if (max_q_len == num_tokens && num_seqs == 1) return cb::launch_prefill_tc(a, main);
+
+  // Mixed step: prefill chunks on the auxiliary stream, decode rows on `stream`.
+  cb::AuxStream* aux = cb::aux_stream();
+  if (!aux) return CB_ERR_CUDA;
+  cb::lock_aux();
+  cudaError_t e = cudaEventRecord(aux->fork, main);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(aux->stream, aux->fork, 0);
+  if (e != cudaSuccess) {
+    cb::unlock_aux();
+    return cb::cuda_fail(e, "forking the auxiliary stream");
+  }
+  cb_status sp = cb::launch_prefill_tc(a, aux->stream);
+  cb_status sd = cb::launch_split_kv(a, false, workspace, workspace_bytes, main);
+  e = cudaEventRecord(aux->join, aux->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(main, aux->join, 0);
+  cb::unlock_aux();
+  if (e != cudaSuccess) return cb::cuda_fail(e, "joining the auxiliary stream");
+  return sp != CB_OK ? sp : sd;
+}

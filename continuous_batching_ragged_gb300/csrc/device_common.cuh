@@ -1,0 +1,78 @@
+// Device-side helpers shared by the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "cb.h"
+
+namespace cb {
+
+// Bits of the per-device error word (see cb_check_device_errors).
+constexpr unsigned kErrBounds = 1u;
+constexpr unsigned kErrTimeout = 2u;
+constexpr unsigned kErrInvalid = 4u;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void raise_error(unsigned* word, unsigned bits) {
+  atomicOr(word, bits);
+}
+
+// 2^x on the special function unit (PTX ex2.approx; ex2(-inf) = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Widen a 16-byte vector of T into fp32 values.
+template <typename T>
+struct Vec16;
+
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void to_float(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+};
+
+template <>
+struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void to_float(const uint4& v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+};
+
+// Round fp32 values to T (bf16: round to nearest even) and store them.
+__device__ __forceinline__ void store_row(__nv_bfloat16* dst, const float* f, int n) {
+  for (int i = 0; i < n; i += 2) {
+    __nv_bfloat162 pr = __floats2bfloat162_rn(f[i], f[i + 1]);
+    *reinterpret_cast<__nv_bfloat162*>(dst + i) = pr;
+  }
+}
+__device__ __forceinline__ void store_row(float* dst, const float* f, int n) {
+  for (int i = 0; i < n; ++i) dst[i] = f[i];
+}
+
+// Read-only 16-byte global load that bypasses L1 allocation (streamed data).
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+}  // namespace cb

@@ -1,0 +1,40 @@
+// Per-device runtime state shared by the entry points.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "host_common.h"
+
+namespace cb {
+
+// Device address of the current device's error word (lazily resolved).
+// Returns nullptr and records an error message on failure.
+unsigned* device_error_word();
+
+// cuTensorMapEncodeTiled from the driver, fetched through the runtime so the
+// library does not link libcuda directly.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// A second stream on the current device plus a fork/join event pair, used to
+// run prefill chunks and decode rows of one step concurrently.  The returned
+// mutex must be held while the events are recorded and waited on.
+struct AuxStream {
+  cudaStream_t stream;
+  cudaEvent_t fork;
+  cudaEvent_t join;
+};
+AuxStream* aux_stream();
+void lock_aux();
+void unlock_aux();
+
+// Number of SMs of the current device.
+int sm_count();
+
+cb_status cuda_fail(cudaError_t err, const char* what);
+
+}  // namespace cb

@@ -1,0 +1,346 @@
+// K2 + K4: split-KV attention of single query rows on CUDA cores, merged by
+// log-sum-exp.
+//
+// Page "continuous-batching" (zhangchitc.github.io), sections "Ragged
+// batching" (a decoding request's one query is dotted with every key it has
+// seen, cache plus its new token) and "Inside the kernel" (the request's cache
+// is read one paged block at a time; each block's scores weight its values and
+// are accumulated into a running state -- online softmax).
+//
+// Decode is HBM-bound (one multiply-add per key byte pair), so the design
+// goal is bytes in flight, not arithmetic:
+//   * grid (split, head, row): a row's keys are cut into fixed 512-key splits,
+//     so a long context spreads over many CTAs;
+//   * 4 warps per CTA, each warp walks 16-key tiles; a lane issues 16-byte
+//     loads, half a warp covers one 256-byte key row, so each load instruction
+//     of the warp reads two whole rows of one paged (block, head) tile;
+//   * the 16-lane dot-product reduction is a transpose-reduce (each shuffle
+//     step halves the rows a lane holds), 8 shuffles for 8 rows instead of 32;
+//   * running max / sum / accumulator per warp, merged across warps in shared
+//     memory, then across splits by the last CTA of the row to finish (an
+//     atomic ticket), which writes the output row.
+#include <cfloat>
+
+#include "device_common.cuh"
+#include "kernels.h"
+#include "runtime.h"
+
+namespace cb {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kTile = 16;   // keys per warp iteration
+
+struct SplitArgs {
+  AttnArgs a;
+  float* partials;          // [rows][H][max_splits][A + 2]
+  int32_t* tickets;         // [rows][H]
+  int32_t max_splits;
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum v[0..N) over the LPR lanes of a row group so that, afterwards, v[0] of
+// lane l holds the full sum of row index  sum_k ((l & (LPR >> k)) ? (N >> k) : 0).
+template <int N, int LPR>
+__device__ __forceinline__ void transpose_reduce(float (&v)[N], int lane) {
+  int cnt = N;
+#pragma unroll
+  for (int bit = LPR / 2; bit >= 1; bit >>= 1) {
+    if (cnt > 1) {
+      const int half = cnt / 2;
+      const bool upper = lane & bit;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < half) {
+          const float send = upper ? v[i] : v[i + half];
+          const float keep = upper ? v[i + half] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+        }
+      }
+      cnt = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], bit);
+    }
+  }
+}
+
+template <typename T, int A, bool ROW_MODE>
+__global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs sa) {
+  constexpr int EPV = Vec16<T>::N;        // elements per 16-byte load
+  constexpr int LPR = A / EPV;            // lanes per key row
+  constexpr int RPL = 32 / LPR;           // key rows per warp load
+  constexpr int NR = kTile / RPL;         // key rows per lane per tile
+  static_assert(NR <= LPR && NR >= 1, "tile shape");
+  const AttnArgs& a = sa.a;
+
+  const int split = blockIdx.x;
+  const int h = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+
+  // ---- which query row, how many keys ------------------------------------
+  int s, t, key_end;
+  if (ROW_MODE) {
+    t = blockIdx.z;
+    int lo = 0, hi = a.num_seqs - 1;
+    while (lo < hi) {                     // last s with cu[s] <= t
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.cu_seqlens_q[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    s = lo;
+  } else {
+    s = blockIdx.z;
+  }
+  const int c0 = a.cu_seqlens_q[s];
+  const int c1 = a.cu_seqlens_q[s + 1];
+  const int q_len = c1 - c0;
+  const int ctx = a.context_lens[s];
+  if (!ROW_MODE) {
+    if (q_len != 1) return;               // prefill chunk: not ours
+    t = c0;
+  }
+  const bool bad = q_len < 1 || ctx < q_len || ctx > a.max_context_len || q_len > a.max_q_len ||
+                   c0 < 0 || c1 > a.num_tokens || (ROW_MODE && (t < c0 || t >= c1)) ||
+                   (ctx + a.block_size - 1) / a.block_size > a.max_blocks_per_seq;
+  if (bad) {
+    if (split == 0 && h == 0 && threadIdx.x == 0) raise_error(a.err, kErrInvalid);
+    return;
+  }
+  key_end = ROW_MODE ? ctx - q_len + (t - c0) + 1 : ctx;
+  const int nsplit = (key_end + kSplitKeys - 1) / kSplitKeys;
+  if (split >= nsplit) return;
+  const int k0 = split * kSplitKeys;
+  const int k1 = min(key_end, k0 + kSplitKeys);
+
+  const int g = lane / LPR;               // which key row of a load this lane covers
+  const int c = lane % LPR;               // which 16-byte chunk of the row
+
+  // q row, pre-scaled by scale * log2(e) so scores are in the exp2 domain
+  float qf[EPV];
+  {
+    const uint4 qv = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) +
+                                                     (size_t(t) * a.num_heads + h) * A + c * EPV);
+    Vec16<T>::to_float(qv, qf);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) qf[e] *= a.scale_log2;
+  }
+
+  const T* kp = static_cast<const T*>(a.k_pool);
+  const T* vp = static_cast<const T*>(a.v_pool);
+  const int32_t* bt = a.block_tables + size_t(s) * a.max_blocks_per_seq;
+  const int B = a.block_size;
+  const size_t head_off = size_t(h) * B * A;
+  const size_t blk_stride = size_t(a.num_heads) * B * A;
+  const bool whole_tiles = (B % kTile) == 0;
+
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[EPV];
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
+
+  for (int base = k0 + warp * kTile; base < k1; base += kWarps * kTile) {
+    uint4 kv[NR], vv[NR];
+    int32_t tile_blk = 0;
+    if (whole_tiles) {
+      tile_blk = bt[base / B];
+      if (tile_blk < 0 || tile_blk >= a.num_blocks) {
+        if (lane == 0) raise_error(a.err, kErrBounds);
+        tile_blk = -1;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      const int j = base + g + RPL * i;
+      kv[i] = make_uint4(0, 0, 0, 0);
+      vv[i] = make_uint4(0, 0, 0, 0);
+      if (j < k1) {
+        int32_t blk = tile_blk;
+        if (!whole_tiles) {
+          blk = bt[j / B];
+          if (blk < 0 || blk >= a.num_blocks) {
+            raise_error(a.err, kErrBounds);
+            blk = -1;
+          }
+        }
+        if (blk >= 0) {
+          const size_t off = size_t(blk) * blk_stride + head_off + size_t(j % B) * A + c * EPV;
+          kv[i] = ldg_stream(kp + off);
+          vv[i] = ldg_stream(vp + off);
+        }
+      }
+    }
+    float sc[NR];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      float kf[EPV];
+      Vec16<T>::to_float(kv[i], kf);
+      float d = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) d = fmaf(qf[e], kf[e], d);
+      sc[i] = d;
+    }
+    transpose_reduce<NR, LPR>(sc, lane);
+    // lane holds the score of tile row g + RPL * idx, idx = (lane % LPR) / (LPR / NR)
+    const int idx = c / (LPR / NR);
+    const int my_row = base + g + RPL * idx;
+    const float sv = my_row < k1 ? sc[0] : -INFINITY;
+    const float m_new = fmaxf(m_run, warp_max(sv));
+    const float alpha = ex2(m_run - m_new);
+    const float pr = ex2(sv - m_new);
+    const float psum = warp_sum((c % (LPR / NR)) == 0 ? pr : 0.f);
+    l_run = l_run * alpha + psum;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[e] *= alpha;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      const float pi = __shfl_sync(0xffffffffu, pr, g * LPR + i * (LPR / NR));
+      float vf[EPV];
+      Vec16<T>::to_float(vv[i], vf);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) acc[e] = fmaf(pi, vf[e], acc[e]);
+    }
+    m_run = m_new;
+  }
+  // lanes of different row groups hold the same chunk: add them
+#pragma unroll
+  for (int o = LPR; o < 32; o <<= 1) {
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+  }
+
+  __shared__ float sm_acc[kWarps][A];
+  __shared__ float sm_m[kWarps], sm_l[kWarps];
+  __shared__ int sm_last;
+  if (g == 0) {
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) sm_acc[warp][c * EPV + e] = acc[e];
+  }
+  if (lane == 0) {
+    sm_m[warp] = m_run;
+    sm_l[warp] = l_run;
+  }
+  __syncthreads();
+
+  const int d = threadIdx.x;
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w]);
+  float L = 0.f, o = 0.f;
+  if (d < A) {
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = ex2(sm_m[w] - M);   // a warp with no keys has m = -inf: weight 0
+      L = fmaf(sm_l[w], f, L);
+      o = fmaf(sm_acc[w][d], f, o);
+    }
+  }
+  T* out_row = static_cast<T*>(a.out) + (size_t(t) * a.num_heads + h) * A;
+  if (nsplit == 1) {
+    if (d < A) {
+      const float r = o / L;
+      store_row(out_row + d, &r, 1);
+    }
+    return;
+  }
+  const int row_id = ROW_MODE ? t : s;
+  float* part = sa.partials + ((size_t(row_id) * a.num_heads + h) * sa.max_splits) * (A + 2);
+  if (d < A) part[size_t(split) * (A + 2) + d] = o;
+  if (d == 0) {
+    part[size_t(split) * (A + 2) + A] = M;
+    part[size_t(split) * (A + 2) + A + 1] = L;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t* ticket = sa.tickets + size_t(row_id) * a.num_heads + h;
+    sm_last = atomicAdd(ticket, 1) == nsplit - 1;
+    if (sm_last) *ticket = 0;             // every split has arrived: reset for the next call
+  }
+  __syncthreads();
+  if (!sm_last) return;
+  __threadfence();
+  if (d < A) {
+    float MM = -INFINITY;
+    for (int k = 0; k < nsplit; ++k) MM = fmaxf(MM, __ldcg(part + size_t(k) * (A + 2) + A));
+    float LL = 0.f, oo = 0.f;
+    for (int k = 0; k < nsplit; ++k) {
+      const float* pk = part + size_t(k) * (A + 2);
+      const float f = ex2(__ldcg(pk + A) - MM);
+      LL = fmaf(__ldcg(pk + A + 1), f, LL);
+      oo = fmaf(__ldcg(pk + d), f, oo);
+    }
+    const float r = oo / LL;
+    store_row(out_row + d, &r, 1);
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+size_t split_kv_workspace_bytes(bool row_mode, int32_t num_seqs, int32_t num_tokens,
+                                int32_t num_heads, int32_t head_dim, int32_t max_context_len) {
+  const size_t rows = size_t(row_mode ? num_tokens : num_seqs);
+  const size_t splits = size_t((max_context_len + kSplitKeys - 1) / kSplitKeys);
+  if (rows == 0 || splits <= 1) return 256;
+  return align256(rows * num_heads * sizeof(int32_t)) +
+         rows * num_heads * splits * (head_dim + 2) * sizeof(float);
+}
+
+template <typename T, int A, bool ROW>
+static void launch(const SplitArgs& sa, dim3 grid, cudaStream_t stream) {
+  split_kv_kernel<T, A, ROW><<<grid, kWarps * 32, 0, stream>>>(sa);
+}
+
+cb_status launch_split_kv(const AttnArgs& a, bool row_mode, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  const int32_t rows = row_mode ? a.num_tokens : a.num_seqs;
+  if (rows == 0) return CB_OK;
+  if (rows > 65535) return fail(CB_ERR_UNSUPPORTED, "split-KV path: more than 65535 rows");
+  SplitArgs sa;
+  sa.a = a;
+  sa.max_splits = (a.max_context_len + kSplitKeys - 1) / kSplitKeys;
+  const size_t need = split_kv_workspace_bytes(row_mode, a.num_seqs, a.num_tokens, a.num_heads,
+                                               a.head_dim, a.max_context_len);
+  if (workspace_bytes < need || (need > 256 && !workspace))
+    return fail(CB_ERR_INVALID, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(CB_ERR_INVALID, "workspace must be 256-byte aligned");
+  sa.tickets = static_cast<int32_t*>(workspace);
+  sa.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         align256(size_t(rows) * a.num_heads * sizeof(int32_t)));
+  if (sa.max_splits > 1) {
+    cudaError_t e = cudaMemsetAsync(workspace, 0, size_t(rows) * a.num_heads * sizeof(int32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing split tickets");
+  }
+  dim3 grid(unsigned(sa.max_splits), unsigned(a.num_heads), unsigned(rows));
+  const bool bf16 = a.dtype == CB_DTYPE_BF16;
+  if (bf16 && a.head_dim == 128) {
+    row_mode ? launch<__nv_bfloat16, 128, true>(sa, grid, stream)
+             : launch<__nv_bfloat16, 128, false>(sa, grid, stream);
+  } else if (bf16 && a.head_dim == 64) {
+    row_mode ? launch<__nv_bfloat16, 64, true>(sa, grid, stream)
+             : launch<__nv_bfloat16, 64, false>(sa, grid, stream);
+  } else if (!bf16 && a.head_dim == 128) {
+    row_mode ? launch<float, 128, true>(sa, grid, stream) : launch<float, 128, false>(sa, grid, stream);
+  } else if (!bf16 && a.head_dim == 64) {
+    row_mode ? launch<float, 64, true>(sa, grid, stream) : launch<float, 64, false>(sa, grid, stream);
+  } else {
+    return fail(CB_ERR_UNSUPPORTED, "split-KV path: head_dim must be 64 or 128");
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "split-KV launch");
+  return CB_OK;
+}
+
+}  // namespace cb

@@ -1,0 +1,210 @@
+/*
+ * cb.h -- C ABI of the ragged continuous-batching attention step on one GPU.
+ *
+ * One step of continuous batching, as the surveyed pages define it:
+ *
+ *   - Hugging Face blog "Continuous batching from first principles", section
+ *     "Continuous batching": sequences are concatenated without padding
+ *     ("ragged batching"); each step holds at most m tokens, decoding requests
+ *     first at one token each, the rest filled by chunked prefill; finished
+ *     requests leave and waiting ones join.
+ *   - page "continuous-batching" (zhangchitc.github.io), section "Inside the
+ *     kernel: cu_seqlens splits six rows back into three": the step's keys and
+ *     values are written into each request's cache entry, then every key and
+ *     value of the request is read back block by block for attention, with an
+ *     online softmax; cu_seqlens delimits each request's rows.
+ *
+ * Conventions for every entry point
+ *   - Device buffers are allocated and owned by the caller.  The library keeps
+ *     no pointer after a call returns.  Attention needs a caller-provided
+ *     workspace (cb_attention_workspace_size).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Device work is enqueued on it and the call returns after the launch.
+ *   - Errors that can be seen on the host (null pointers, sizes, unsupported
+ *     dtype/shape combinations, bounds given by the caller) are returned before
+ *     anything is launched.  Errors that only the device can see (a slot or
+ *     block id outside the pool, metadata that contradicts the host bounds, a
+ *     bounded wait that ran out) set a per-device error word instead: the
+ *     offending work item is skipped and cb_check_device_errors reports it.
+ *   - No C++ exception crosses the ABI.  cb_last_error() describes the most
+ *     recent failure of a call made on the calling thread.
+ *   - Head-major paged cache: K and V are separate pools, each
+ *     [num_blocks][num_heads][block_size][head_dim], row-major.  Token slot
+ *     s = block_id * block_size + offset lives at pool[block_id][h][offset][:].
+ *     Packed token tensors (q, k_new, v_new, out) are [num_tokens][num_heads]
+ *     [head_dim], row-major.
+ */
+#ifndef CB_H_
+#define CB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CB_OK = 0,
+  CB_ERR_INVALID = 1,      /* bad argument or metadata */
+  CB_ERR_BOUNDS = 2,       /* a slot or block id outside the pool (device) */
+  CB_ERR_NO_BLOCKS = 3,    /* scheduler: request can never fit the pool */
+  CB_ERR_TIMEOUT = 4,      /* a bounded device wait ran out (device) */
+  CB_ERR_CUDA = 5,         /* a CUDA runtime call failed */
+  CB_ERR_UNSUPPORTED = 6   /* dtype / head_dim / block_size combination not built */
+} cb_status;
+
+typedef enum { CB_DTYPE_F32 = 0, CB_DTYPE_BF16 = 1 } cb_dtype;
+
+/* One layer's paged KV cache.  k and v point to device pools of
+ * num_blocks * num_heads * block_size * head_dim elements of `dtype`, each
+ * 16-byte aligned.  Caller-owned. */
+typedef struct {
+  void* k;
+  void* v;
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_heads;
+  int32_t head_dim;
+  cb_dtype dtype;
+} cb_kv_cache;
+
+/* ---------------------------------------------------------------------------
+ * cb_append_kv -- write this step's keys and values into the cache.
+ * Page "continuous-batching" (zhangchitc.github.io), section "Inside the
+ * kernel": the new keys and values are written into the KV cache, each into
+ * its own request's entry, before attention reads the cache back.
+ *
+ *   k_new, v_new  device [num_tokens][num_heads][head_dim] of cache->dtype,
+ *                 16-byte aligned.
+ *   slot_mapping  device int64 [num_tokens]; token t goes to slot
+ *                 slot_mapping[t]; a negative slot skips the token.
+ *   A slot >= num_blocks * block_size sets CB_ERR_BOUNDS on the device word and
+ *   is not written.  head_dim * element size must be a multiple of 16 bytes.
+ * ------------------------------------------------------------------------- */
+cb_status cb_append_kv(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                       int32_t num_tokens, const cb_kv_cache* cache, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * cb_ragged_attention -- attention of one packed, padding-free step.
+ * Hugging Face blog "Continuous batching from first principles", sections
+ * "Attention" (masked row-wise softmax of Q K^T times V), "Chunked prefill"
+ * (a chunk sees the cached keys of its earlier tokens plus itself, causally)
+ * and "Continuous batching" (concatenated sequences never see each other);
+ * page "continuous-batching", section "Ragged batching" (a decoding request's
+ * one query against all of its keys, a prefilling request's causal block).
+ *
+ * Sequence s owns packed rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1 (q_len_s
+ * >= 1 rows) and has context_lens[s] keys in the cache AFTER this step's
+ * append, so p_s = context_lens[s] - q_len_s were cached before the step.
+ * Its row i (0-based) attends keys j = 0 .. p_s + i:
+ *     out = softmax_j(scale * q . k_j) v_j,   accumulated in fp32.
+ *
+ *   q             device [num_tokens][H][A] of cache->dtype.
+ *   cu_seqlens_q  device int32 [num_seqs + 1], cu[0] = 0, cu[num_seqs] = num_tokens.
+ *   context_lens  device int32 [num_seqs].
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]; logical block b
+ *                 of sequence s is physical block block_tables[s][b].  Entries
+ *                 past ceil(context_lens[s] / block_size) are never read.
+ *   max_q_len, max_context_len  host upper bounds over the batch; the device
+ *                 flags (CB_ERR_INVALID) and skips any sequence exceeding them.
+ *   out           device [num_tokens][H][A] of cache->dtype; every row written.
+ *   workspace     device scratch of at least cb_attention_workspace_size(...)
+ *                 bytes, 256-byte aligned, used by split-KV decoding; its
+ *                 contents need no initialisation and are not preserved.
+ *   Concurrent calls must not share one workspace.
+ * Built combinations: bf16 with head_dim 128 and block_size in {8,16,32,64,128}
+ * (prefill chunks on tcgen05 tensor cores, decode rows split-KV on CUDA cores);
+ * f32 with head_dim 64 or 128 and any block_size (every row on CUDA cores).
+ * ------------------------------------------------------------------------- */
+size_t cb_attention_workspace_size(const cb_kv_cache* cache, int32_t num_seqs,
+                                   int32_t num_tokens, int32_t max_context_len);
+
+cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache,
+                              const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                              const int32_t* block_tables, int32_t num_seqs, int32_t num_tokens,
+                              int32_t max_blocks_per_seq, int32_t max_q_len,
+                              int32_t max_context_len, float scale, void* out,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Host scheduler: one iteration-level step at a time.
+ * hassanahmed.net "How Continuous Batching Speeds Up LLM Serving", the
+ * scheduler loop: drop finished requests and release their KV blocks, admit
+ * waiting requests while they fit, run exactly one forward pass; Hugging Face
+ * blog, section "Continuous batching": budget of m tokens, decoding requests
+ * first at one token each, the remaining room filled by chunked prefill.
+ *
+ * Rules where the pages leave the step open: waiting requests are ordered by
+ * (arrival_step, id) and admitted strictly FIFO when arrived, under
+ * max_num_seqs (0 = no cap) and with ceil((prompt_len + output_len) /
+ * block_size) unreserved blocks (the whole lifetime is reserved at admission);
+ * decode tokens go in admission order; prefill room is filled greedily in
+ * admission order; blocks are handed out lowest free id first; a request is
+ * finished after output_len tokens (the prefill pass yields the first) and is
+ * evicted at the start of the next cb_build_batch.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int32_t token_budget;   /* m = max tokens per step (max_num_batched_tokens) */
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_num_seqs;   /* 0 = unlimited */
+} cb_sched_config;
+
+typedef struct cb_scheduler cb_scheduler;
+
+/* Host arrays owned by the scheduler, valid until its next cb_build_batch or
+ * cb_scheduler_destroy.  Sequences are listed decode first, then prefill. */
+typedef struct {
+  int32_t num_seqs;
+  int32_t num_tokens;           /* T = sum of q_lens <= token_budget */
+  int32_t num_decode;           /* the first num_decode sequences have q_len 1 */
+  int32_t max_blocks_per_seq;   /* row stride of block_tables */
+  int32_t max_q_len;
+  int32_t max_context_len;
+  const int32_t* cu_seqlens_q;  /* [num_seqs + 1] */
+  const int32_t* context_lens;  /* [num_seqs] */
+  const int32_t* block_tables;  /* [num_seqs][max_blocks_per_seq], -1 padded */
+  const int64_t* slot_mapping;  /* [num_tokens] */
+  const int64_t* request_ids;   /* [num_seqs] */
+  int32_t num_evicted;
+  const int64_t* evicted_ids;   /* [num_evicted], evicted by this call */
+} cb_batch;
+
+typedef struct {
+  int64_t step;                 /* completed steps */
+  int32_t num_waiting;
+  int32_t num_running;          /* includes finished requests not yet evicted */
+  int32_t free_blocks;
+  int32_t reserved_blocks;
+  int64_t num_finished;         /* evicted so far */
+} cb_sched_stats;
+
+cb_status cb_scheduler_create(const cb_sched_config* config, cb_scheduler** out);
+void cb_scheduler_destroy(cb_scheduler* sched);
+/* CB_ERR_NO_BLOCKS if the request could never be admitted (needs more blocks
+ * than the pool holds); CB_ERR_INVALID for prompt_len < 1, output_len < 1,
+ * arrival_step < 0 or an id already known. */
+cb_status cb_add_request(cb_scheduler* sched, int64_t id, int64_t arrival_step,
+                         int32_t prompt_len, int32_t output_len);
+/* Evict, admit, choose this step's tokens, allocate blocks, emit metadata.
+ * CB_ERR_INVALID if the previous batch was not completed. */
+cb_status cb_build_batch(cb_scheduler* sched, cb_batch* out);
+/* Account the last batch as run: cached tokens, output tokens, the clock. */
+cb_status cb_complete_step(cb_scheduler* sched);
+cb_status cb_scheduler_stats(const cb_scheduler* sched, cb_sched_stats* out);
+
+/* ---------------------------------------------------------------------------
+ * Errors.
+ * cb_check_device_errors synchronises `stream`, reads and clears the current
+ * device's error word and returns CB_ERR_TIMEOUT, CB_ERR_BOUNDS or
+ * CB_ERR_INVALID (in that order of precedence) if any was raised since the
+ * last check, else CB_OK.
+ * ------------------------------------------------------------------------- */
+cb_status cb_check_device_errors(void* stream);
+const char* cb_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CB_H_ */

@@ -11,3 +11,11 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+@pytest.fixture(scope="session")
+def native_lib():
+    """Build (if stale) and load libcb.so; its host functions need no GPU."""
+    from continuous_batching_ragged_gb300 import build, native
+    build.build()
+    return native.lib()
