@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Benchmark of one ragged continuous-batching attention step on GB300.
+
+A step is the whole hot path over one packed batch: the step's K/V appended
+to the paged cache (cb_append_kv), then attention of every packed query row
+(cb_ragged_attention: split-KV decode rows on CUDA cores and prefill chunks
+on tcgen05 tensor cores, concurrently).  The default workload is the decode
+step (256 sequences, one query each, cached contexts uniform in [512, 4096],
+32 heads x 128, bf16, block 16, blocks randomly permuted in the pool);
+--workload picks the others.  Inputs are seeded synthetic values generated
+in HBM before timing; the KV cache (9.7 GB for the decode step) is far larger
+than L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ragged-attention step tokens/s on 1 GB300; % HBM / tensor roofline per step"
+UNIT = "tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def make_workload(name: str):
+    from continuous_batching_ragged_gb300 import workloads as W
+    if name == "decode":
+        return W.decode_step(), "decode_256seq_ctx512-4096_bf16_H32_A128_B16"
+    if name == "mixed":
+        return W.mixed_step(), "mixed_m2048_64decode_ctx256-4096_chunks661-661-662_bf16_H32_A128_B16"
+    if name == "long":
+        return W.long_prompt_chunk(15), "long_prompt_32768_last_chunk_2048_bf16_H32_A128_B16"
+    if name == "tiny":
+        return W.tiny_fp32(), "tiny_fp32_H4_A64_B4_T6"
+    raise SystemExit(f"unknown workload {name}")
+
+
+def algorithmic_work(b):
+    """Bytes and flops counted once (each KV byte read once, masked pairs not counted)."""
+    e = b.elem_bytes
+    H, A = b.num_heads, b.head_dim
+    kv_read = int(np.sum(b.context_lens.astype(np.int64))) * 2 * H * A * e
+    qo = b.T * H * A * e * 2
+    append = 2 * 2 * b.T * H * A * e
+    pairs = sum(int(q) * int(p) + int(q) * (int(q) + 1) // 2 for p, q in zip(b.p, b.q_len))
+    flops = 4 * A * H * pairs
+    decode = b.q_len == 1
+    dec_bytes = (int(np.sum(b.context_lens[decode].astype(np.int64))) * 2 * H * A * e
+                 + int(np.sum(decode)) * H * A * e * 2)
+    return {"bytes": kv_read + qo + append, "flops": flops, "decode_bytes": dec_bytes,
+            "append_bytes": append,
+            "prefill_flops": 4 * A * H * sum(int(q) * int(p) + int(q) * (int(q) + 1) // 2
+                                             for p, q in zip(b.p, b.q_len) if q > 1)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# device staging (inputs generated in HBM by the seeded device generator)
+# ---------------------------------------------------------------------------
+
+class Staged:
+    def __init__(self, b, torch, api, W):
+        dt = torch.bfloat16 if b.dtype == "bf16" else torch.float32
+        self.b = b
+        self.cache = api.KVCache.empty(b.num_blocks, b.num_heads, b.block_size, b.head_dim, dt)
+        self.cache.k.zero_()
+        self.cache.v.zero_()
+        sid = torch.from_numpy(b.seq_ids).cuda()
+        if int(b.p.max()) > 0:
+            pl = torch.from_numpy(b.p.astype(np.int32)).cuda()
+            bt = torch.from_numpy(b.block_tables).cuda()
+            for kind, pool in ((W.KIND_K, self.cache.k), (W.KIND_V, self.cache.v)):
+                api.cb_synth_fill_cache(pool, b.seed, kind, b.layer, sid, pl, bt, int(b.p.max()))
+        rows = torch.from_numpy(np.repeat(b.seq_ids, b.q_len)).cuda()
+        pos = torch.from_numpy(np.concatenate(
+            [np.arange(b.p[s], b.p[s] + b.q_len[s]) for s in range(b.num_seqs)]).astype(np.int32)).cuda()
+        shape = (b.T, b.num_heads, b.head_dim)
+        self.q, self.k_new, self.v_new = (torch.empty(shape, dtype=dt, device="cuda") for _ in range(3))
+        for kind, t in ((W.KIND_Q, self.q), (W.KIND_K, self.k_new), (W.KIND_V, self.v_new)):
+            api.cb_synth_tokens(t, b.seed, kind, b.layer, rows, pos)
+        self.cu = torch.from_numpy(b.cu_seqlens_q).cuda()
+        self.ctx = torch.from_numpy(b.context_lens).cuda()
+        self.bt = torch.from_numpy(b.block_tables).cuda()
+        self.slots = torch.from_numpy(b.slot_mapping).cuda()
+        self.out = torch.empty_like(self.q)
+        ws = api.cb_attention_workspace_size(self.cache, b.num_seqs, b.T, b.max_context_len)
+        self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device="cuda")
+        self.scale = 1.0 / math.sqrt(b.head_dim)
+        self.api = api
+
+    def append(self, stream=None, k=None, v=None, slots=None):
+        self.api.cb_append_kv(self.k_new if k is None else k, self.v_new if v is None else v,
+                              self.slots if slots is None else slots, self.cache, stream)
+
+    def attend(self, stream=None, q=None, cu=None, ctx=None, bt=None, out=None):
+        b = self.b
+        self.api.cb_ragged_attention(self.q if q is None else q, self.cache,
+                                     self.cu if cu is None else cu, self.ctx if ctx is None else ctx,
+                                     self.bt if bt is None else bt, max_q_len=b.max_q_len,
+                                     max_context_len=b.max_context_len, scale=self.scale,
+                                     out=self.out if out is None else out, workspace=self.ws,
+                                     stream=stream)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+# ---------------------------------------------------------------------------
+
+_RANDOM_CACHE = {}
+
+
+def _random_inputs(n_max, c_max, H, A):
+    key = (n_max, c_max, H, A)
+    if key not in _RANDOM_CACHE:
+        rng = np.random.default_rng(0)
+        _RANDOM_CACHE.clear()
+        _RANDOM_CACHE[key] = (rng.standard_normal((n_max, H, A)), rng.standard_normal((c_max, H, A)),
+                              rng.standard_normal((c_max, H, A)))
+    return _RANDOM_CACHE[key]
+
+
+def time_oracle(b, budget_s: float):
+    """Time the oracle (as it stands) on a bounded sample of the workload's
+    sequences, with random inputs of the workload's shapes (drawn once and
+    sliced per sequence; drawing them is not timed).  Returns (tokens/s,
+    sample description, cores, seconds spent)."""
+    from oracle import attention as oa
+    H, A = b.num_heads, b.head_dim
+    scale = 1.0 / math.sqrt(A)
+    qbuf, kbuf, vbuf = _random_inputs(b.max_q_len, b.max_context_len, H, A)
+    order = np.argsort(-b.q_len, kind="stable")          # prefill chunks first, then decodes
+    done_tokens, done_seqs, spent = 0, 0, 0.0
+    for s in order:
+        n, c = int(b.q_len[s]), int(b.context_lens[s])
+        t0 = time.perf_counter()
+        oa.attend_sequence(qbuf[:n], kbuf[:c], vbuf[:c], c - n, scale)
+        spent += time.perf_counter() - t0
+        done_tokens += n
+        done_seqs += 1
+        if spent >= budget_s:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"{done_seqs} of {b.num_seqs} sequences ({done_tokens} of {b.T} query tokens, all "
+              f"{H} heads), fp64 numpy, random inputs of the workload's shapes")
+    return done_tokens / spent, sample, cores, spent
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_reference(args, b, label):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    per_step = []
+    tokens, cores = 0, 1
+    sample = ""
+    budget = max(0.2, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup + args.steps):
+        tps, sample, cores, spent = time_oracle(b, budget)
+        if i >= args.warmup:
+            per_step.append(tps)
+    value = statistics.median(per_step)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": b.T / value * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": label, "num_seqs": b.num_seqs,
+                                            "tokens_per_step": b.T},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "mixed", "long", "tiny"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    b, label = make_workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, b, label)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from continuous_batching_ragged_gb300 import build as _build
+    _build.build()
+    from continuous_batching_ragged_gb300 import api
+    from continuous_batching_ragged_gb300 import workloads as W
+
+    rank, world, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev_index = torch.cuda.current_device()
+
+    st = Staged(b, torch, api, W)
+    stream = torch.cuda.current_stream()
+    work = algorithmic_work(b)
+    peaks = load_peaks()
+
+    # warm-up (also checks the device error word once)
+    for _ in range(args.warmup):
+        st.append()
+        st.attend()
+    api.cb_check_device_errors()
+    torch.cuda.synchronize()
+
+    launches_per_step = 2 + (1 if b.max_q_len > 1 and np.any(b.q_len == 1) else 0)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(dev_index)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        st.append()
+        ev[i][1].record(stream)
+        st.attend()
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    api.cb_check_device_errors()
+    total_ms = t_start.elapsed_time(t_end)
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * b.T / (ms * 1e-3)
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # step's inputs and metadata, the two calls, D2H of the output
+    host = {name: getattr(st, name).cpu().pin_memory() for name in
+            ("q", "k_new", "v_new", "cu", "ctx", "bt", "slots")}
+    dev_in = {name: torch.empty_like(getattr(st, name)) for name in host}
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_steps = max(10, args.steps // 3)
+
+    def e2e_step():
+        for name, t in host.items():
+            dev_in[name].copy_(t, non_blocking=True)
+        st.append(k=dev_in["k_new"], v=dev_in["v_new"], slots=dev_in["slots"])
+        st.attend(q=dev_in["q"], cu=dev_in["cu"], ctx=dev_in["ctx"], bt=dev_in["bt"])
+        out_host.copy_(st.out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    api.cb_check_device_errors()
+
+    # roofline of the dominant kernel and of the whole step
+    if b.max_q_len == 1 or args.workload == "decode":
+        dom = {"kernel": "split_kv_kernel (decode rows)", "bound": "hbm",
+               "achieved": work["decode_bytes"] / (attn_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+               "unit": "GB/s"}
+    else:
+        dom = {"kernel": "prefill_tc_kernel (prefill chunks)", "bound": "tensor",
+               "achieved": work["prefill_flops"] / (attn_ms * 1e-3) / 1e12,
+               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    dom["frac"] = dom["achieved"] / dom["peak"]
+    dom["traffic"] = None
+    dom["peak_source"] = f"of {peaks['source']}"
+    t_hbm = work["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = work["flops"] / (peaks["bf16_tflops"] * 1e12)
+    step_roof = {"bytes": work["bytes"], "flops": work["flops"],
+                 "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                 "roofline_ms": max(t_hbm, t_tc) * 1e3, "measured_ms": ms,
+                 "frac": max(t_hbm, t_tc) * 1e3 / ms,
+                 "frac_vs_nominal_8tbs": (work["bytes"] / (NOMINAL_HBM_GBS * 1e9)) * 1e3 / ms,
+                 "append_ms": append_ms, "attention_ms": attn_ms}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tps, sample, cores, _ = time_oracle(b, args.cpu_budget)
+        cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": b.dtype, "data": "synthetic",
+                "config": {"workload": label, "num_seqs": b.num_seqs, "tokens_per_step": b.T,
+                           "kv_bytes_read": int(work["bytes"] - work["append_bytes"]),
+                           "l2": "inputs larger than L2 (KV cache read per step >> 129 MB)"
+                           if work["bytes"] > 1e9 else "inputs smaller than L2; no flush",
+                           "parallelism": "replicas" if world > 1 else "single GPU"},
+                "roofline": dom, "step_roofline": step_roof, "cpu_baseline": cpu,
+                "e2e": {"value": world * b.T / (e2e_ms * 1e-3), "unit": UNIT,
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "clocks": clocks, "gpu_launches": launches_per_step * args.steps}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -55,16 +55,9 @@ struct Vec16<float> {
   }
 };
 
-// Round fp32 values to T (bf16: round to nearest even) and store them.
-__device__ __forceinline__ void store_row(__nv_bfloat16* dst, const float* f, int n) {
-  for (int i = 0; i < n; i += 2) {
-    __nv_bfloat162 pr = __floats2bfloat162_rn(f[i], f[i + 1]);
-    *reinterpret_cast<__nv_bfloat162*>(dst + i) = pr;
-  }
-}
-__device__ __forceinline__ void store_row(float* dst, const float* f, int n) {
-  for (int i = 0; i < n; ++i) dst[i] = f[i];
-}
+// Round one fp32 value to T (bf16: round to nearest even) and store it.
+__device__ __forceinline__ void store1(__nv_bfloat16* dst, float v) { *dst = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void store1(float* dst, float v) { *dst = v; }
 
 // Read-only 16-byte global load that bypasses L1 allocation (streamed data).
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {

@@ -1,11 +1,394 @@
-// K3: prefill-chunk attention on tcgen05 tensor cores (placeholder).
+// K3: prefill-chunk attention on tcgen05 tensor cores (bf16, head_dim 128).
+//
+// Hugging Face blog "Continuous batching from first principles", section
+// "Chunked prefill": a chunk's queries see the keys and values stored for the
+// earlier tokens of the prompt plus the chunk's own, with the causal mask
+// shifted accordingly; section "Attention": scores Q K^T, mask, row softmax,
+// times V.  Page "continuous-batching" (zhangchitc.github.io), section
+// "Inside the kernel": the request's cache is read one paged block at a time
+// and each block's contribution is accumulated into a running state (online
+// softmax).
+//
+// One CTA computes one tile of 128 query rows of one (sequence, head):
+//   * warp 4 (TMA): loads the Q tile once, then K and V tiles of 128 keys into
+//     a 2-stage ring; a 128-key tile is 128/B paged blocks, each one 3-D TMA
+//     box [B rows x 64 dims] per 64-dim half, 128-byte swizzled.  Blocks past
+//     the context are requested at an out-of-range coordinate, which TMA fills
+//     with zeros.
+//   * warp 5 (MMA): one thread issues S = Q K^T (8 x K16 MMAs, fp32 in TMEM
+//     columns 0-127), then O += P V (A operand P read from TMEM columns
+//     256-319, V as an N-contiguous B operand), committing to mbarriers.
+//   * warps 0-3 (softmax): thread i owns query row i = TMEM lane i.  It loads
+//     its 128 scores, masks keys j > p + i (p = cached length), keeps a running
+//     max in the exp2 domain (rescaling O in TMEM only when the max grew by
+//     more than 2^8, so most tiles skip the O round trip), writes P as bf16 to
+//     TMEM, and at the end normalises O and stores its row.
+// The S MMA of tile j+1 is issued as soon as the softmax has read tile j's
+// scores, so it overlaps the P V MMA of tile j and the softmax's exp work.
+// Every mbarrier wait is bounded; a timeout sets the device error word and
+// the CTA winds down, freeing its TMEM.
+#include <cuda.h>
+
+#include "device_common.cuh"
 #include "kernels.h"
 #include "runtime.h"
+#include "sm100_ptx.cuh"
 
 namespace cb {
+namespace {
 
-cb_status launch_prefill_tc(const AttnArgs&, cudaStream_t) {
-  return fail(CB_ERR_UNSUPPORTED, "prefill chunks on tensor cores are not built yet");
+using namespace sm100;
+
+constexpr int BM = 128;                          // query rows per tile = TMEM lanes
+constexpr int BN = 128;                          // keys per KV tile
+constexpr int HD = 128;                          // head dim
+constexpr int kStages = 2;                       // K/V ring depth
+constexpr int kThreads = 192;                    // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr uint32_t kHalf = BM * 64 * 2;          // one 64-dim swizzled half: 16 KB
+constexpr uint32_t kTile = 2 * kHalf;            // a 128 x 128 bf16 tile: 32 KB
+constexpr uint32_t kColS = 0, kColO = 128, kColP = 256, kTmemCols = 512;
+
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kTile;
+constexpr uint32_t kOffV = kOffK + kStages * kTile;
+constexpr uint32_t kOffBar = kOffV + kStages * kTile;
+enum : int {
+  BAR_Q = 0,
+  BAR_S = 1,
+  BAR_P = 2,
+  BAR_O = 3,
+  BAR_KF = 4,
+  BAR_VF = BAR_KF + kStages,
+  BAR_KVE = BAR_VF + kStages,
+  NUM_BARS = BAR_KVE + kStages
+};
+constexpr uint32_t kOffTmemSlot = kOffBar + 8 * NUM_BARS;
+constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;   // + slack to align the base to 1 KB
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    tmem_ld32(taddr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
+  const int qt = gridDim.x - 1 - blockIdx.x;       // the longest tiles launch first
+  const int h = blockIdx.y;
+  const int s = blockIdx.z;
+  const int c0 = a.cu_seqlens_q[s];
+  const int c1 = a.cu_seqlens_q[s + 1];
+  const int q_len = c1 - c0;
+  if (q_len == 1) return;                          // a decode row: the split-KV kernel's
+  const int ctx = a.context_lens[s];
+  const int B = a.block_size;
+  const bool bad = q_len < 1 || ctx < q_len || ctx > a.max_context_len || q_len > a.max_q_len ||
+                   c0 < 0 || c1 > a.num_tokens || (ctx + B - 1) / B > a.max_blocks_per_seq;
+  if (bad) {
+    if (qt == 0 && h == 0 && threadIdx.x == 0) raise_error(a.err, kErrInvalid);
+    return;
+  }
+  const int row0 = qt * BM;
+  if (row0 >= q_len) return;
+  const int p = ctx - q_len;                       // cached tokens before this step
+  const int kv_end = min(p + row0 + BM, ctx);      // keys any row of this tile can see
+  const int n_tiles = (kv_end + BN - 1) / BN;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;    // 128B-swizzled tiles need 1 KB alignment
+  uint8_t* gsm = smem_raw + (base - raw);
+  auto bar = [&](int i) -> uint32_t { return base + kOffBar + 8u * uint32_t(i); };
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(BAR_Q), 1);
+    mbar_init(bar(BAR_S), 1);
+    mbar_init(bar(BAR_P), BM);
+    mbar_init(bar(BAR_O), 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(bar(BAR_KF + st), 1);
+      mbar_init(bar(BAR_VF + st), 1);
+      mbar_init(bar(BAR_KVE + st), 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(base + kOffTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gsm + kOffTmemSlot);
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar(BAR_Q), kTile);
+      tma_load_3d(base + kOffQ, &tm_q, bar(BAR_Q), 0, h, c0 + row0);
+      tma_load_3d(base + kOffQ + kHalf, &tm_q, bar(BAR_Q), 64, h, c0 + row0);
+      const int bpt = BN / B;                      // paged blocks per KV tile
+      const int32_t* bt = a.block_tables + size_t(s) * a.max_blocks_per_seq;
+      const int oob = a.num_blocks * a.num_heads;  // first out-of-range box index: zero fill
+      int z[16];
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % kStages;
+        if (j >= kStages && !mbar_wait(bar(BAR_KVE + st), ((j / kStages) - 1) & 1)) {
+          raise_error(a.err, kErrTimeout);
+          break;
+        }
+        for (int bi = 0; bi < bpt; ++bi) {
+          const int lb = j * bpt + bi;
+          z[bi] = oob;
+          if (lb * B < ctx) {
+            const int blk = bt[lb];
+            if (blk >= 0 && blk < a.num_blocks) z[bi] = blk * a.num_heads + h;
+            else raise_error(a.err, kErrBounds);
+          }
+        }
+        const uint32_t kdst = base + kOffK + st * kTile;
+        const uint32_t vdst = base + kOffV + st * kTile;
+        mbar_arrive_expect_tx(bar(BAR_KF + st), kTile);
+        for (int bi = 0; bi < bpt; ++bi) {
+          tma_load_3d(kdst + bi * B * 128, &tm_k, bar(BAR_KF + st), 0, 0, z[bi]);
+          tma_load_3d(kdst + kHalf + bi * B * 128, &tm_k, bar(BAR_KF + st), 64, 0, z[bi]);
+        }
+        mbar_arrive_expect_tx(bar(BAR_VF + st), kTile);
+        for (int bi = 0; bi < bpt; ++bi) {
+          tma_load_3d(vdst + bi * B * 128, &tm_v, bar(BAR_VF + st), 0, 0, z[bi]);
+          tma_load_3d(vdst + kHalf + bi * B * 128, &tm_v, bar(BAR_VF + st), 64, 0, z[bi]);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);   // Q (K-major) x K (K-major)
+      constexpr uint32_t idO = idesc_bf16_f32(BM, HD, true);    // P (TMEM) x V (N-contiguous)
+      const uint32_t tS = tmem + kColS, tO = tmem + kColO, tP = tmem + kColP;
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kStages;
+        if (!mbar_wait(bar(BAR_KF + st), (j / kStages) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kb = base + kOffK + st * kTile;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
+          mma_f16_ss(tS, smem_desc(base + kOffQ + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS,
+                     k > 0);
+        }
+        mma_commit(bar(BAR_S));
+        return true;
+      };
+      bool ok = mbar_wait(bar(BAR_Q), 0) && issue_s(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (!mbar_wait(bar(BAR_P), j & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (j + 1 < n_tiles && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        const int st = j % kStages;
+        if (!mbar_wait(bar(BAR_VF + st), (j / kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vb = base + kOffV + st * kTile;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          mma_f16_ts(tO, tP + k * 8, smem_desc(vb + k * 2048, kHalf, 1024), idO, (j > 0 || k > 0));
+        mma_commit(bar(BAR_O));
+        mma_commit(bar(BAR_KVE + st));
+      }
+      if (!ok) raise_error(a.err, kErrTimeout);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int i = threadIdx.x;                     // tile row = TMEM lane
+    const int qi = row0 + i;                       // row within the chunk
+    const int limit = min(p + qi, ctx - 1);        // last key this row sees
+    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+    const float sl2 = a.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!mbar_wait(bar(BAR_S), j & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld128(lane_base + kColS, sr);
+      tmem_wait_ld();
+      const int kb = j * BN;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        const float v = kb + c <= limit ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
+        sr[c] = __float_as_uint(v);
+        mt = fmaxf(mt, v);
+      }
+      const float m_new = fmaxf(m, mt);
+      const bool resc = m_new > m + 8.0f;         // keep a stale max while exp2 stays <= 2^8
+      const float m_use = resc ? m_new : m;
+      const float alpha = resc ? ex2(m - m_new) : 1.0f;
+      float rs = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = ex2(__uint_as_float(sr[2 * c]) - m_use);
+        const float p1 = ex2(__uint_as_float(sr[2 * c + 1]) - m_use);
+        rs += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + rs;
+      m = m_use;
+      tc_fence_before();
+      if (j > 0) {                                 // P V of tile j-1 done: P free, O stable
+        if (!mbar_wait(bar(BAR_O), (j - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + kColO + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(lane_base + kColO + 32 * c, o);
+          }
+        }
+      }
+      tmem_st32(lane_base + kColP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(lane_base + kColP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_wait_st();
+      if (j == n_tiles - 1) {
+        // Rows of the last paged block past the context hold stale cache bytes;
+        // P is 0 there but 0 * NaN is NaN, so zero those V rows (whole blocks
+        // past the context already arrived as TMA zero fill).
+        const int r0 = ctx - kb;
+        const int r1 = min(BN, ((ctx + B - 1) / B) * B - kb);
+        if (r0 < r1) {
+          const int st = j % kStages;
+          if (!mbar_wait(bar(BAR_VF + st), (j / kStages) & 1)) {
+            ok = false;
+            break;
+          }
+          uint8_t* vt = gsm + kOffV + st * kTile;
+          const int chunks = (r1 - r0) * 16;       // 16-byte chunks over both halves
+          for (int c = i; c < chunks; c += BM) {
+            const int r = r0 + c / 16, w = c % 16;
+            *reinterpret_cast<uint4*>(vt + (w / 8) * kHalf + r * 128 + (w % 8) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(BAR_P));
+    }
+    if (ok && mbar_wait(bar(BAR_O), (n_tiles - 1) & 1)) {
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + (size_t(c0 + qi) * a.num_heads + h) * HD;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + kColO + 32 * c, o);
+        tmem_wait_ld();
+        if (qi < q_len) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float* f = reinterpret_cast<const float*>(&o[8 * e]);
+            d4[e] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                               pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+          }
+        }
+      }
+    } else if (ok) {
+      ok = false;
+    }
+    if (!ok && lane == 0) raise_error(a.err, kErrTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+bool g_attr_set[64] = {};
+
+}  // namespace
+
+cb_status launch_prefill_tc(const AttnArgs& a, cudaStream_t stream) {
+  if (a.dtype != CB_DTYPE_BF16 || a.head_dim != HD)
+    return fail(CB_ERR_UNSUPPORTED, "prefill chunks: bf16 with head_dim 128 only");
+  const int B = a.block_size;
+  if (B < 8 || B > BN || (B & (B - 1)) != 0)
+    return fail(CB_ERR_UNSUPPORTED, "prefill chunks: block_size must be a power of two in [8, 128]");
+  if (a.num_seqs > 65535 || a.num_heads > 65535)
+    return fail(CB_ERR_UNSUPPORTED, "prefill chunks: more than 65535 sequences or heads");
+  if (int64_t(a.num_blocks) * a.num_heads >= (int64_t(1) << 31))
+    return fail(CB_ERR_UNSUPPORTED, "prefill chunks: num_blocks * num_heads must fit in int32");
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return CB_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  const cuuint32_t ones[3] = {1, 1, 1};
+  {
+    const cuuint64_t dims[3] = {cuuint64_t(HD), cuuint64_t(a.num_heads), cuuint64_t(a.num_tokens)};
+    const cuuint64_t strides[2] = {cuuint64_t(HD) * 2, cuuint64_t(a.num_heads) * HD * 2};
+    const cuuint32_t box[3] = {64, 1, cuuint32_t(BM)};
+    CUresult r = enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box,
+                     ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(CB_ERR_CUDA, "encoding the Q tensor map failed (%d)", int(r));
+  }
+  {
+    const cuuint64_t dims[3] = {cuuint64_t(HD), cuuint64_t(B), cuuint64_t(a.num_blocks) * a.num_heads};
+    const cuuint64_t strides[2] = {cuuint64_t(HD) * 2, cuuint64_t(B) * HD * 2};
+    const cuuint32_t box[3] = {64, cuuint32_t(B), 1};
+    CUresult r = enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k_pool), dims, strides,
+                     box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS)
+      r = enc(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.v_pool), dims, strides, box,
+              ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(CB_ERR_CUDA, "encoding the KV tensor maps failed (%d)", int(r));
+  }
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+    if (e != cudaSuccess) return cuda_fail(e, "prefill chunks: shared memory attribute");
+    g_attr_set[dev] = true;
+  }
+  const dim3 grid(unsigned((a.max_q_len + BM - 1) / BM), unsigned(a.num_heads), unsigned(a.num_seqs));
+  prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "prefill chunks: launch");
+  return CB_OK;
 }
 
 }  // namespace cb

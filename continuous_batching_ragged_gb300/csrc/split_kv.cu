@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs s
   const int q_len = c1 - c0;
   const int ctx = a.context_lens[s];
   if (!ROW_MODE) {
-    if (q_len != 1) return;               // prefill chunk: not ours
+    if (q_len > 1) return;                // prefill chunk: not ours
     t = c0;
   }
   const bool bad = q_len < 1 || ctx < q_len || ctx > a.max_context_len || q_len > a.max_q_len ||
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs s
   if (nsplit == 1) {
     if (d < A) {
       const float r = o / L;
-      store_row(out_row + d, &r, 1);
+      store1(out_row + d, r);
     }
     return;
   }
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs s
       oo = fmaf(__ldcg(pk + d), f, oo);
     }
     const float r = oo / LL;
-    store_row(out_row + d, &r, 1);
+    store1(out_row + d, r);
   }
 }
 

@@ -1,0 +1,153 @@
+"""Prefill chunks on tcgen05 (and mixed steps) against the oracle, plus the
+invariants the pages state: chunked == single pass, packed == alone,
+incremental decode == recompute, no leakage."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from continuous_batching_ragged_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("B", [16, 8, 64, 128])
+def test_prefill_chunks_small(native_lib, B):
+    """Chunk lengths around the 128-row tile, cached prefixes around the
+    128-key tile and block edges; the pool's unused slots hold NaN."""
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_packed, to_np
+    p = [0, 0, 5, 16, 127, 128, 1000, 3]
+    q = [2, 128, 127, 129, 300, 64, 33, 1]
+    b = W.make_batch(p, q, num_heads=2, head_dim=128, block_size=B, dtype="bf16", seed=50 + B)
+    got = to_np(DeviceStep(b).run())
+    assert_tolerance(got, oracle_packed(b))
+
+
+def test_mixed_step_scaled_down(native_lib):
+    """Decode rows and prefill chunks in one step (both kernels concurrently)."""
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_packed, to_np
+    b = W.mixed_step(num_decode=12, ctx_lo=100, ctx_hi=700, chunks=(61, 130, 200),
+                     chunk_p=(0, 129, 300), num_heads=4, seed=7)
+    got = to_np(DeviceStep(b).run())
+    assert_tolerance(got, oracle_packed(b))
+
+
+def test_mixed_step_full_size_sampled(native_lib):
+    """The full mixed step: 64 decode rows (contexts 256-4096) plus chunks of
+    661/661/662 rows at cached lengths 0/1024/2048, 32 heads; sampled rows of
+    every prefill chunk and of 16 decode sequences against the oracle."""
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_rows, to_np
+    b = W.mixed_step()
+    out = to_np(DeviceStep(b, source="device").run())
+    assert np.all(np.isfinite(out))
+    rng = np.random.default_rng(3)
+    got, exp = [], []
+    cu = b.cu_seqlens_q
+    for s in range(b.num_seqs - 3, b.num_seqs):
+        rows = sorted(set(rng.choice(int(b.q_len[s]), 12, replace=False).tolist()) | {0, int(b.q_len[s]) - 1})
+        heads = sorted(rng.choice(32, 2, replace=False).tolist())
+        exp.append(oracle_rows(b, s, heads, rows).reshape(-1, b.head_dim))
+        got.append(out[cu[s] + np.array(rows)][:, heads].reshape(-1, b.head_dim))
+    for s in rng.choice(b.num_seqs - 3, 16, replace=False):
+        heads = sorted(rng.choice(32, 2, replace=False).tolist())
+        exp.append(oracle_rows(b, int(s), heads).reshape(-1, b.head_dim))
+        got.append(out[cu[s]:cu[s] + 1][:, heads].reshape(-1, b.head_dim))
+    assert_tolerance(np.concatenate(got), np.concatenate(exp))
+
+
+def _run_chunked_prompt(prompt, chunk, H=32, seed=3):
+    """Process one prompt chunk by chunk through append + attention on one
+    cache; returns (cache, output of the last chunk)."""
+    from gpu_harness import DeviceStep
+    cache = None
+    st = None
+    for k in range(prompt // chunk):
+        b = W.long_prompt_chunk(k, seed=seed, prompt=prompt, chunk=chunk, num_heads=H)
+        st = DeviceStep(b, source="device", cache=cache) if cache is not None else DeviceStep(b, source="device")
+        cache = st.cache
+        st.run()
+    return st
+
+
+def test_long_prompt_chunked_equals_single_pass(native_lib):
+    """A 32768-token prompt in 16 chunks of 2048, each appended and attended
+    over the paged cache; the last chunk equals rows 30720.. of one pass over
+    all 32768 tokens, and sampled rows match the oracle."""
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_rows, to_np
+    prompt, chunk = 32768, 2048
+    last = _run_chunked_prompt(prompt, chunk)
+    got_last = last.out.clone()
+    single_b = W.long_prompt_chunk(0, prompt=prompt, chunk=chunk, single_pass=True)
+    single = DeviceStep(single_b, source="device")
+    single.run()
+    ref_rows = single.out[prompt - chunk:]
+    # same 128-row tiles and 128-key tiles in both runs: identical arithmetic
+    assert torch.equal(got_last.view(torch.int16), ref_rows.view(torch.int16))
+    rng = np.random.default_rng(1)
+    rows = sorted(set(rng.choice(chunk, 10, replace=False).tolist()) | {0, chunk - 1})
+    heads = [0, 17]
+    b_last = last.b
+    exp = oracle_rows(b_last, 0, heads, rows)
+    got = to_np(got_last)[np.array(rows)][:, heads]
+    assert_tolerance(got, exp)
+
+
+def test_prefill_packed_equals_alone_bitwise(native_lib):
+    from gpu_harness import DeviceStep
+    b = W.make_batch([0, 300, 5, 40], [200, 1, 77, 1], num_heads=2, head_dim=128, block_size=16,
+                     dtype="bf16", seed=61)
+    full = DeviceStep(b)
+    out = full.run().clone()
+    cu = b.cu_seqlens_q
+    for s in range(b.num_seqs):
+        sub = W.RaggedBatch(num_heads=2, head_dim=128, block_size=16, dtype="bf16", seed=61, layer=0,
+                            seq_ids=b.seq_ids[s:s + 1], p=b.p[s:s + 1], q_len=b.q_len[s:s + 1],
+                            block_tables=b.block_tables[s:s + 1], num_blocks=b.num_blocks)
+        st = DeviceStep(sub, cache=full.cache)
+        st.attend()
+        torch.cuda.synchronize()
+        assert torch.equal(st.out.view(torch.int16), out[cu[s]:cu[s + 1]].view(torch.int16))
+
+
+def test_prefill_no_cross_sequence_leakage(native_lib):
+    from gpu_harness import DeviceStep
+    b = W.make_batch([10, 0, 200], [150, 90, 40], num_heads=2, head_dim=128, block_size=16,
+                     dtype="bf16", seed=71)
+    st = DeviceStep(b)
+    base = st.run().clone()
+    cu = b.cu_seqlens_q
+    for s in (0, 2):
+        blk = torch.from_numpy(b.block_tables[s][b.block_tables[s] >= 0]).long().cuda()
+        st.cache.k[blk] = st.cache.k[blk] * -2
+        st.cache.v[blk] = st.cache.v[blk] + 3
+        st.q[cu[s]:cu[s + 1]] *= 3
+    st.attend()
+    torch.cuda.synchronize()
+    assert torch.equal(st.out[cu[1]:cu[2]].view(torch.int16), base[cu[1]:cu[2]].view(torch.int16))
+    assert not torch.equal(st.out[cu[0]:cu[1]], base[cu[0]:cu[1]])
+
+
+def test_incremental_decode_matches_single_pass(native_lib):
+    """KV cache: prefill 300 tokens, then decode 5 tokens one step at a time;
+    each decode row matches the corresponding row of a single causal pass."""
+    from gpu_harness import DeviceStep, assert_tolerance, to_np
+    P, D, H = 300, 5, 4
+    total = P + D
+    ids = np.random.default_rng(0).permutation(64).astype(np.int32)
+    bt = ids[:math.ceil(total / 16)].reshape(1, -1)
+
+    def batch(p, q):
+        return W.RaggedBatch(num_heads=H, head_dim=128, block_size=16, dtype="bf16", seed=81, layer=0,
+                             seq_ids=np.zeros(1, np.int64), p=np.array([p]), q_len=np.array([q]),
+                             block_tables=bt.copy(), num_blocks=64)
+
+    st = DeviceStep(batch(0, P))
+    st.run()
+    dec = []
+    for t in range(P, total):
+        s2 = DeviceStep(batch(t, 1), cache=st.cache)
+        dec.append(to_np(s2.run())[0])
+    full = DeviceStep(batch(0, total))
+    ref = to_np(full.run())[P:]
+    assert_tolerance(np.stack(dec), ref)
