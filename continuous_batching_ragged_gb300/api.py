@@ -110,6 +110,20 @@ def cb_ragged_attention(q: torch.Tensor, cache: KVCache, cu_seqlens_q: torch.Ten
     return out
 
 
+def cb_decode_attention_noalloc(q: torch.Tensor, cache: KVCache, cu_seqlens_q: torch.Tensor,
+                                context_lens: torch.Tensor, block_tables: torch.Tensor, *,
+                                max_context_len: int, scale: float, out: torch.Tensor,
+                                stream=None) -> torch.Tensor:
+    """Decode-only attention whose scratch is a fixed array the library reserves
+    in device memory, for callers that cannot allocate or lend a workspace."""
+    c = cache.c_struct()
+    check(native.lib().cb_decode_attention_noalloc(
+        _ptr(q), ctypes.byref(c), _ptr(cu_seqlens_q), _ptr(context_lens), _ptr(block_tables),
+        context_lens.shape[0], q.shape[0], block_tables.shape[1], max_context_len, float(scale),
+        _ptr(out), _stream_handle(stream)), "cb_decode_attention_noalloc")
+    return out
+
+
 def cb_check_device_errors(stream=None) -> None:
     check(native.lib().cb_check_device_errors(_stream_handle(stream)), "cb_check_device_errors")
 

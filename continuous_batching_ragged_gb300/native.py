@@ -15,9 +15,11 @@ CB_OK, CB_ERR_INVALID, CB_ERR_BOUNDS, CB_ERR_NO_BLOCKS, CB_ERR_TIMEOUT, CB_ERR_C
 STATUS_NAMES = {0: "CB_OK", 1: "CB_ERR_INVALID", 2: "CB_ERR_BOUNDS", 3: "CB_ERR_NO_BLOCKS",
                 4: "CB_ERR_TIMEOUT", 5: "CB_ERR_CUDA", 6: "CB_ERR_UNSUPPORTED"}
 CB_DTYPE_F32, CB_DTYPE_BF16 = 0, 1
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024      # CB_NOALLOC_SCRATCH_BYTES in cb.h
 
 # Every entry point declared in the public headers.
 EXPORTS = ("cb_append_kv", "cb_attention_workspace_size", "cb_ragged_attention",
+           "cb_decode_attention_noalloc",
            "cb_scheduler_create", "cb_scheduler_destroy", "cb_add_request", "cb_build_batch",
            "cb_complete_step", "cb_scheduler_stats", "cb_check_device_errors", "cb_last_error",
            "cb_synth_tokens", "cb_synth_fill_cache")
@@ -73,6 +75,7 @@ def lib() -> ctypes.CDLL:
         "cb_append_kv": (st, [vp, vp, vp, i32, pcache, vp]),
         "cb_attention_workspace_size": (sz, [pcache, i32, i32, i32]),
         "cb_ragged_attention": (st, [vp, pcache, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, sz, vp]),
+        "cb_decode_attention_noalloc": (st, [vp, pcache, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]),
         "cb_scheduler_create": (st, [ctypes.POINTER(cb_sched_config), ctypes.POINTER(vp)]),
         "cb_scheduler_destroy": (None, [vp]),
         "cb_add_request": (st, [vp, i64, i64, i32, i32]),

@@ -128,6 +128,38 @@ cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * cb_decode_attention_noalloc -- decode attention that allocates nothing.
+ * The paper has no counterpart: this is a deployment variant of the decode
+ * rows of cb_ragged_attention for callers that cannot allocate device memory
+ * and have no workspace to lend -- for example an op running inside a host
+ * framework whose caching allocator (or a KV pool sized to fill the GPU)
+ * already owns all device memory, behind a plugin interface that passes only
+ * the op's inputs and outputs.
+ *
+ * Same arguments and result as cb_ragged_attention for a step in which every
+ * sequence has exactly one query token (num_tokens == num_seqs, max_q_len 1),
+ * without the workspace.  The split-KV scratch lives instead in one array of
+ * CB_NOALLOC_SCRATCH_BYTES that the library reserves in device memory on every
+ * GPU that loads it, until the process exits.  A step whose scratch would not
+ * fit (the size cb_attention_workspace_size reports for it) is rejected with
+ * CB_ERR_INVALID before anything is launched.
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents;
+ *     the call clears what must start at zero itself.  Calls whose GPU work
+ *     overlaps (several streams or host threads) race on it and corrupt each
+ *     other's results: serialise them, e.g. on one stream.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ * ------------------------------------------------------------------------- */
+#define CB_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+cb_status cb_decode_attention_noalloc(const void* q, const cb_kv_cache* cache,
+                                      const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                      const int32_t* block_tables, int32_t num_seqs,
+                                      int32_t num_tokens, int32_t max_blocks_per_seq,
+                                      int32_t max_context_len, float scale, void* out,
+                                      void* stream);
+
+/* ---------------------------------------------------------------------------
  * Host scheduler: one iteration-level step at a time.
  * hassanahmed.net "How Continuous Batching Speeds Up LLM Serving", the
  * scheduler loop: drop finished requests and release their KV blocks, admit
