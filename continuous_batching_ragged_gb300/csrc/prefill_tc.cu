@@ -9,22 +9,23 @@
 // and each block's contribution is accumulated into a running state (online
 // softmax).
 //
-// One CTA computes one tile of 128 query rows of one (sequence, head):
-//   * warp 4 (TMA): loads the Q tile once, then K and V tiles of 128 keys into
-//     a 2-stage ring; a 128-key tile is 128/B paged blocks, each one 3-D TMA
-//     box [B rows x 64 dims] per 64-dim half, 128-byte swizzled.  Blocks past
-//     the context are requested at an out-of-range coordinate, which TMA fills
-//     with zeros.
-//   * warp 5 (MMA): one thread issues S = Q K^T (8 x K16 MMAs, fp32 in TMEM
-//     columns 0-127), then O += P V (A operand P read from TMEM columns
-//     256-319, V as an N-contiguous B operand), committing to mbarriers.
-//   * warps 0-3 (softmax): thread i owns query row i = TMEM lane i.  It loads
-//     its 128 scores, masks keys j > p + i (p = cached length), keeps a running
-//     max in the exp2 domain (rescaling O in TMEM only when the max grew by
-//     more than 2^8, so most tiles skip the O round trip), writes P as bf16 to
-//     TMEM, and at the end normalises O and stores its row.
-// The S MMA of tile j+1 is issued as soon as the softmax has read tile j's
-// scores, so it overlaps the P V MMA of tile j and the softmax's exp work.
+// One CTA computes two 128-row query tiles of one (sequence, head); the two
+// tiles share every K/V tile loaded into shared memory, and each tile's
+// softmax overlaps the other tile's MMAs on the tensor core.
+//   * warp 8 (TMA): loads both Q tiles once, then K and V tiles of 128 keys
+//     into a 2-stage ring; a 128-key tile is 128/B paged blocks, each one 3-D
+//     TMA box [B rows x 64 dims] per 64-dim half, 128-byte swizzled.  Blocks
+//     past the context are requested at an out-of-range coordinate, which TMA
+//     fills with zeros.
+//   * warp 9 (MMA): one thread issues, per KV tile j and query tile t,
+//     S_t = Q_t K_j^T (fp32 in TMEM) and O_t += P_t V_j (P_t read from TMEM,
+//     V as an N-contiguous B operand).  P_t overwrites the first 64 columns of
+//     S_t, so S_t(j+1) is issued only once P_t V_j has completed.
+//   * warps 0-3 / 4-7 (softmax of tile 0 / 1): thread i owns query row i =
+//     TMEM lane i.  It loads its 128 scores, masks keys j > p + i only on the
+//     tiles that cross its warp's diagonal, keeps a running max in the exp2
+//     domain (rescaling O in TMEM only when the max grew by more than 2^8),
+//     writes P as bf16 into TMEM, and at the end normalises O and stores.
 // Every mbarrier wait is bounded; a timeout sets the device error word and
 // the CTA winds down, freeing its TMEM.
 #include <cuda.h>
@@ -42,22 +43,24 @@ using namespace sm100;
 constexpr int BM = 128;                          // query rows per tile = TMEM lanes
 constexpr int BN = 128;                          // keys per KV tile
 constexpr int HD = 128;                          // head dim
+constexpr int kQTiles = 2;                       // query tiles per CTA
 constexpr int kStages = 2;                       // K/V ring depth
-constexpr int kThreads = 192;                    // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kThreads = 320;                    // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr uint32_t kHalf = BM * 64 * 2;          // one 64-dim swizzled half: 16 KB
 constexpr uint32_t kTile = 2 * kHalf;            // a 128 x 128 bf16 tile: 32 KB
-constexpr uint32_t kColS = 0, kColO = 128, kColP = 256, kTmemCols = 512;
+constexpr uint32_t kTmemCols = 512;              // per tile t: S at 256t, O at 256t + 128
 
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTile;
+constexpr uint32_t kOffK = kOffQ + kQTiles * kTile;
 constexpr uint32_t kOffV = kOffK + kStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kStages * kTile;
 enum : int {
   BAR_Q = 0,
-  BAR_S = 1,
-  BAR_P = 2,
-  BAR_O = 3,
-  BAR_KF = 4,
+  BAR_S = 1,                  // + t
+  BAR_P = BAR_S + kQTiles,    // + t
+  BAR_O = BAR_P + kQTiles,    // + t
+  BAR_KF = BAR_O + kQTiles,   // + stage
   BAR_VF = BAR_KF + kStages,
   BAR_KVE = BAR_VF + kStages,
   NUM_BARS = BAR_KVE + kStages
@@ -80,7 +83,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
-  const int qt = gridDim.x - 1 - blockIdx.x;       // the longest tiles launch first
+  const int qp = gridDim.x - 1 - blockIdx.x;       // the longest tile pairs launch first
   const int h = blockIdx.y;
   const int s = blockIdx.z;
   const int c0 = a.cu_seqlens_q[s];
@@ -92,13 +95,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool bad = q_len < 1 || ctx < q_len || ctx > a.max_context_len || q_len > a.max_q_len ||
                    c0 < 0 || c1 > a.num_tokens || (ctx + B - 1) / B > a.max_blocks_per_seq;
   if (bad) {
-    if (qt == 0 && h == 0 && threadIdx.x == 0) raise_error(a.err, kErrInvalid);
+    if (qp == 0 && h == 0 && threadIdx.x == 0) raise_error(a.err, kErrInvalid);
     return;
   }
-  const int row0 = qt * BM;
+  const int row0 = qp * kQTiles * BM;             // first chunk row of tile 0
   if (row0 >= q_len) return;
+  const int nq = row0 + BM < q_len ? 2 : 1;        // tiles of this pair holding real rows
   const int p = ctx - q_len;                       // cached tokens before this step
-  const int kv_end = min(p + row0 + BM, ctx);      // keys any row of this tile can see
+  const int kv_end = min(p + row0 + nq * BM, ctx); // keys any row of the pair can see
   const int n_tiles = (kv_end + BN - 1) / BN;
 
   extern __shared__ uint8_t smem_raw[];
@@ -111,9 +115,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
-    mbar_init(bar(BAR_S), 1);
-    mbar_init(bar(BAR_P), BM);
-    mbar_init(bar(BAR_O), 1);
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(bar(BAR_S + t), 1);
+      mbar_init(bar(BAR_P + t), BM);
+      mbar_init(bar(BAR_O + t), 1);
+    }
     for (int st = 0; st < kStages; ++st) {
       mbar_init(bar(BAR_KF + st), 1);
       mbar_init(bar(BAR_VF + st), 1);
@@ -121,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(base + kOffTmemSlot, kTmemCols);
     tmem_relinquish();
   }
@@ -129,15 +135,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gsm + kOffTmemSlot);
 
-  if (warp == 4) {
+  if (warp == kWarpTma) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar(BAR_Q), kTile);
-      tma_load_3d(base + kOffQ, &tm_q, bar(BAR_Q), 0, h, c0 + row0);
-      tma_load_3d(base + kOffQ + kHalf, &tm_q, bar(BAR_Q), 64, h, c0 + row0);
+      mbar_arrive_expect_tx(bar(BAR_Q), kQTiles * kTile);
+      for (int t = 0; t < kQTiles; ++t) {
+        tma_load_3d(base + kOffQ + t * kTile, &tm_q, bar(BAR_Q), 0, h, c0 + row0 + t * BM);
+        tma_load_3d(base + kOffQ + t * kTile + kHalf, &tm_q, bar(BAR_Q), 64, h, c0 + row0 + t * BM);
+      }
       const int bpt = BN / B;                      // paged blocks per KV tile
       const int32_t* bt = a.block_tables + size_t(s) * a.max_blocks_per_seq;
       const int oob = a.num_blocks * a.num_heads;  // first out-of-range box index: zero fill
@@ -171,96 +179,120 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);   // Q (K-major) x K (K-major)
       constexpr uint32_t idO = idesc_bf16_f32(BM, HD, true);    // P (TMEM) x V (N-contiguous)
-      const uint32_t tS = tmem + kColS, tO = tmem + kColO, tP = tmem + kColP;
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kStages;
-        if (!mbar_wait(bar(BAR_KF + st), (j / kStages) & 1)) return false;
-        tc_fence_after();
-        const uint32_t kb = base + kOffK + st * kTile;
+      auto issue_s = [&](int t, int j) {
+        const uint32_t kb = base + kOffK + (j % kStages) * kTile;
+        const uint32_t qb = base + kOffQ + t * kTile;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
-          mma_f16_ss(tS, smem_desc(base + kOffQ + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS,
+          mma_f16_ss(tmem + 256 * t, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS,
                      k > 0);
         }
-        mma_commit(bar(BAR_S));
-        return true;
+        mma_commit(bar(BAR_S + t));
       };
-      bool ok = mbar_wait(bar(BAR_Q), 0) && issue_s(0);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (!mbar_wait(bar(BAR_P), j & 1)) {
-          ok = false;
-          break;
-        }
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t vb = base + kOffV + (j % kStages) * kTile;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          mma_f16_ts(tmem + 256 * t + 128, tmem + 256 * t + k * 8, smem_desc(vb + k * 2048, kHalf, 1024),
+                     idO, (j > 0 || k > 0));
+        mma_commit(bar(BAR_O + t));
+      };
+      bool ok = mbar_wait(bar(BAR_Q), 0) && mbar_wait(bar(BAR_KF), 0);
+      if (ok) {
         tc_fence_after();
-        if (j + 1 < n_tiles && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
+        for (int t = 0; t < nq; ++t) issue_s(t, 0);
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j % kStages;
         if (!mbar_wait(bar(BAR_VF + st), (j / kStages) & 1)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t vb = base + kOffV + st * kTile;
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          mma_f16_ts(tO, tP + k * 8, smem_desc(vb + k * 2048, kHalf, 1024), idO, (j > 0 || k > 0));
-        mma_commit(bar(BAR_O));
+        for (int t = 0; t < nq; ++t) {
+          if (!mbar_wait(bar(BAR_P + t), j & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, j);
+        }
+        if (!ok) break;
         mma_commit(bar(BAR_KVE + st));
+        if (j + 1 < n_tiles) {
+          if (!mbar_wait(bar(BAR_KF + (j + 1) % kStages), ((j + 1) / kStages) & 1)) {
+            ok = false;
+            break;
+          }
+          for (int t = 0; t < nq; ++t) {
+            // P_t lives in S_t's columns: wait for P_t V_j before overwriting them
+            if (!mbar_wait(bar(BAR_O + t), j & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, j + 1);
+          }
+        }
       }
       if (!ok) raise_error(a.err, kErrTimeout);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int i = threadIdx.x;                     // tile row = TMEM lane
-    const int qi = row0 + i;                       // row within the chunk
+    const int t = warp >> 2;                       // query tile of this warpgroup
+    const int wq = warp & 3;                       // TMEM lane quarter
+    const int i = threadIdx.x - BM * t;            // tile row = TMEM lane
+    const int qi = row0 + BM * t + i;              // row within the chunk
     const int limit = min(p + qi, ctx - 1);        // last key this row sees
-    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+    const int warp_limit = min(p + row0 + BM * t + 32 * wq, ctx - 1);   // smallest in the warp
+    const uint32_t lane_base = tmem + (uint32_t(wq * 32) << 16) + 256 * t;
     const float sl2 = a.scale_log2;
     float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!mbar_wait(bar(BAR_S), j & 1)) {
+    bool ok = t < nq;
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      if (!mbar_wait(bar(BAR_S + t), j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[128];
-      tmem_ld128(lane_base + kColS, sr);
+      tmem_ld128(lane_base, sr);
       tmem_wait_ld();
       const int kb = j * BN;
       float mt = -INFINITY;
+      if (kb + BN - 1 <= warp_limit) {             // every key of the tile visible to the warp
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        const float v = kb + c <= limit ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
-        sr[c] = __float_as_uint(v);
-        mt = fmaxf(mt, v);
+        for (int c = 0; c < BN; ++c) mt = fmaxf(mt, __uint_as_float(sr[c]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const float v = kb + c <= limit ? __uint_as_float(sr[c]) : -INFINITY;
+          sr[c] = __float_as_uint(v);
+          mt = fmaxf(mt, v);
+        }
       }
-      const float m_new = fmaxf(m, mt);
+      const float m_new = fmaxf(m, mt * sl2);
       const bool resc = m_new > m + 8.0f;         // keep a stale max while exp2 stays <= 2^8
       const float m_use = resc ? m_new : m;
       const float alpha = resc ? ex2(m - m_new) : 1.0f;
       float rs = 0.f;
-      uint32_t pk[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2(__uint_as_float(sr[2 * c]) - m_use);
-        const float p1 = ex2(__uint_as_float(sr[2 * c + 1]) - m_use);
+      for (int c = 0; c < 64; ++c) {               // P packed in place over the scores
+        const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
+        const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
         rs += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+        sr[c] = pack_bf16x2(p0, p1);
       }
       l = l * alpha + rs;
       m = m_use;
       tc_fence_before();
-      if (j > 0) {                                 // P V of tile j-1 done: P free, O stable
-        if (!mbar_wait(bar(BAR_O), (j - 1) & 1)) {
+      if (j > 0) {                                 // P_t V of tile j-1 done: S_t cols free, O_t stable
+        if (!mbar_wait(bar(BAR_O + t), (j - 1) & 1)) {
           ok = false;
           break;
         }
@@ -269,21 +301,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
-            tmem_ld32(lane_base + kColO + 32 * c, o);
+            tmem_ld32(lane_base + 128 + 32 * c, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(lane_base + kColO + 32 * c, o);
+            tmem_st32(lane_base + 128 + 32 * c, o);
           }
         }
       }
-      tmem_st32(lane_base + kColP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(lane_base + kColP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_st32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_st();
-      if (j == n_tiles - 1) {
+      if (t == 0 && j == n_tiles - 1) {
         // Rows of the last paged block past the context hold stale cache bytes;
         // P is 0 there but 0 * NaN is NaN, so zero those V rows (whole blocks
-        // past the context already arrived as TMA zero fill).
+        // past the context already arrived as TMA zero fill).  Tile 0's P V is
+        // issued first, so this also covers tile 1.
         const int r0 = ctx - kb;
         const int r1 = min(BN, ((ctx + B - 1) / B) * B - kb);
         if (r0 < r1) {
@@ -302,35 +335,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(bar(BAR_P));
+      mbar_arrive(bar(BAR_P + t));
     }
-    if (ok && mbar_wait(bar(BAR_O), (n_tiles - 1) & 1)) {
-      tc_fence_after();
-      const float inv = 1.0f / l;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + (size_t(c0 + qi) * a.num_heads + h) * HD;
+    if (ok) {
+      if (mbar_wait(bar(BAR_O + t), (n_tiles - 1) & 1)) {
+        tc_fence_after();
+        const float inv = 1.0f / l;
+        __nv_bfloat16* dst =
+            static_cast<__nv_bfloat16*>(a.out) + (size_t(c0 + qi) * a.num_heads + h) * HD;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + kColO + 32 * c, o);
-        tmem_wait_ld();
-        if (qi < q_len) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + 128 + 32 * c, o);
+          tmem_wait_ld();
+          if (qi < q_len) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float* f = reinterpret_cast<const float*>(&o[8 * e]);
-            d4[e] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
-                               pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+            for (int e = 0; e < 4; ++e) {
+              const float* f = reinterpret_cast<const float*>(&o[8 * e]);
+              d4[e] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                                 pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+            }
           }
         }
+      } else if (lane == 0) {
+        raise_error(a.err, kErrTimeout);
       }
-    } else if (ok) {
-      ok = false;
+    } else if (t < nq && lane == 0) {
+      raise_error(a.err, kErrTimeout);
     }
-    if (!ok && lane == 0) raise_error(a.err, kErrTimeout);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -384,7 +422,9 @@ cb_status launch_prefill_tc(const AttnArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "prefill chunks: shared memory attribute");
     g_attr_set[dev] = true;
   }
-  const dim3 grid(unsigned((a.max_q_len + BM - 1) / BM), unsigned(a.num_heads), unsigned(a.num_seqs));
+  const int rows_per_cta = kQTiles * BM;
+  const dim3 grid(unsigned((a.max_q_len + rows_per_cta - 1) / rows_per_cta), unsigned(a.num_heads),
+                  unsigned(a.num_seqs));
   prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill chunks: launch");
