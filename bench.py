@@ -223,6 +223,109 @@ def time_oracle(b, budget_s: float):
 
 
 # ---------------------------------------------------------------------------
+# serving trace: the scheduler drives every step
+# ---------------------------------------------------------------------------
+
+def run_trace(torch, api, W, requests, *, num_layers, num_heads, head_dim, block_size,
+              token_budget, num_blocks, seed, on_layer=None, max_steps=100000):
+    """Serve ``requests`` to completion.  Each step: cb_build_batch on the host,
+    metadata to the device, then per layer the step's Q/K/V (device generator,
+    keyed by request id and position, not timed) followed by the timed
+    cb_append_kv + cb_ragged_attention on that layer's cache.  Returns per-step
+    records (tokens, host scheduler seconds, device attention milliseconds)."""
+    dt = torch.bfloat16
+    caches = [api.KVCache.empty(num_blocks, num_heads, block_size, head_dim, dt)
+              for _ in range(num_layers)]
+    for c in caches:
+        c.k.zero_()
+        c.v.zero_()
+    sched = api.Scheduler(token_budget, block_size, num_blocks)
+    for r in requests:
+        sched.add_request(r.id, r.arrival_step, r.prompt_len, r.output_len)
+    scale = 1.0 / math.sqrt(head_dim)
+    ws = torch.empty(0, dtype=torch.uint8, device="cuda")
+    qkv = None
+    steps = []
+    stream = torch.cuda.current_stream()
+    for step in range(max_steps):
+        t0 = time.perf_counter()
+        bt = sched.build_batch()
+        t_sched = time.perf_counter() - t0
+        S, T = bt.num_seqs, bt.T
+        if S == 0:
+            t0 = time.perf_counter()
+            sched.complete_step()
+            t_sched += time.perf_counter() - t0
+            if sched.idle:
+                break
+            steps.append({"T": 0, "sched_s": t_sched, "gpu_ms": 0.0})
+            continue
+        q_lens = bt.q_lens
+        rows = np.repeat(bt.request_ids, q_lens)
+        pos = np.concatenate([np.arange(c - q, c) for c, q in zip(bt.context_lens, q_lens)])
+        d_rows = torch.from_numpy(rows.astype(np.int64)).cuda()
+        d_pos = torch.from_numpy(pos.astype(np.int32)).cuda()
+        cu = torch.from_numpy(bt.cu_seqlens_q).cuda()
+        ctx = torch.from_numpy(bt.context_lens).cuda()
+        btab = torch.from_numpy(bt.block_tables).cuda()
+        slots = torch.from_numpy(bt.slot_mapping).cuda()
+        need = api.cb_attention_workspace_size(caches[0], S, T, bt.max_context_len)
+        if need > ws.numel():
+            ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        if qkv is None or qkv[0].shape[0] < T:
+            qkv = [torch.empty((max(T, token_budget), num_heads, head_dim), dtype=dt, device="cuda")
+                   for _ in range(4)]
+        q, k, v, out = (t[:T] for t in qkv)
+        events = []
+        for layer in range(num_layers):
+            for kind, t in ((W.KIND_Q, q), (W.KIND_K, k), (W.KIND_V, v)):
+                api.cb_synth_tokens(t, seed, kind, layer, d_rows, d_pos)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            api.cb_append_kv(k, v, slots, caches[layer])
+            api.cb_ragged_attention(q, caches[layer], cu, ctx, btab, max_q_len=bt.max_q_len,
+                                    max_context_len=bt.max_context_len, scale=scale, out=out,
+                                    workspace=ws)
+            e1.record(stream)
+            events.append((e0, e1))
+            if on_layer is not None:       # runs in stream order, before the next layer reuses `out`
+                on_layer(step, layer, bt, out)
+        torch.cuda.synchronize()
+        gpu_ms = sum(e0.elapsed_time(e1) for e0, e1 in events)
+        api.cb_check_device_errors()
+        t0 = time.perf_counter()
+        sched.complete_step()
+        t_sched += time.perf_counter() - t0
+        steps.append({"T": T, "S": S, "decode": bt.num_decode, "sched_s": t_sched, "gpu_ms": gpu_ms,
+                      "kv_tokens": int(np.sum(bt.context_lens)), "q_lens": q_lens,
+                      "max_q_len": bt.max_q_len,
+                      "ctx": bt.context_lens})
+    del caches
+    torch.cuda.empty_cache()
+    return steps
+
+
+def launches_per_layer(st):
+    """Kernels cb_append_kv + cb_ragged_attention launch for one layer of a step."""
+    prefill = st["max_q_len"] > 1
+    decode = not prefill or not (st["S"] == 1 and st["max_q_len"] == st["T"])
+    return 1 + int(prefill) + int(decode)
+
+
+def trace_step_roofline(step, num_layers, num_heads, head_dim, peaks):
+    """Roofline time of one step over all layers (SURVEY.md-style algorithmic bytes/flops)."""
+    e = 2
+    H, A = num_heads, head_dim
+    ctx = step["ctx"].astype(np.int64)
+    q = step["q_lens"].astype(np.int64)
+    p = ctx - q
+    bytes_ = int(ctx.sum()) * 2 * H * A * e + step["T"] * H * A * e * 2 + 4 * step["T"] * H * A * e
+    flops = 4 * A * H * int(np.sum(q * p + q * (q + 1) // 2))
+    t = max(bytes_ / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops_sustained"] * 1e12))
+    return num_layers * t * 1e3, num_layers * bytes_, num_layers * flops
+
+
+# ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
 
@@ -257,19 +360,92 @@ def run_reference(args, b, label):
     print(json.dumps(line), flush=True)
 
 
+def run_trace_bench(args):
+    """The serving trace end to end: 2000 requests, 32 layers, budget 4096."""
+    from continuous_batching_ragged_gb300 import workloads as W
+    cfg = W.SERVING_TRACE
+    reqs = W.serving_trace()
+    label = (f"serving_trace_{len(reqs)}req_{cfg['num_layers']}layers_m{cfg['token_budget']}_"
+             f"{cfg['num_blocks']}blocks_bf16_H32_A128_B16")
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # the oracle on one mid-trace step's batch (one layer), as a bounded sample
+        from oracle.scheduler import Scheduler as OS
+        o = OS(cfg["token_budget"], cfg["block_size"], cfg["num_blocks"])
+        for r in reqs:
+            o.add_request(r.id, r.arrival_step, r.prompt_len, r.output_len)
+        batch = None
+        for _ in range(60):
+            batch = o.build_batch()
+            o.complete_step()
+        b = W.RaggedBatch(num_heads=cfg["num_heads"], head_dim=cfg["head_dim"],
+                          block_size=cfg["block_size"], dtype="bf16", seed=4, layer=0,
+                          seq_ids=batch.request_ids, p=(batch.context_lens - batch.q_lens).astype(np.int64),
+                          q_len=batch.q_lens.astype(np.int64), block_tables=batch.block_tables,
+                          num_blocks=cfg["num_blocks"])
+        run_reference(args, b, label)
+        return
+    import torch
+    from continuous_batching_ragged_gb300 import build as _build
+    _build.build()
+    from continuous_batching_ragged_gb300 import api
+    torch.cuda.set_device(local)
+    peaks = load_peaks()
+    kw = dict(num_layers=cfg["num_layers"], num_heads=cfg["num_heads"], head_dim=cfg["head_dim"],
+              block_size=cfg["block_size"], token_budget=cfg["token_budget"],
+              num_blocks=cfg["num_blocks"], seed=4)
+    # warm-up: a short trace of the first requests
+    run_trace(torch, api, W, reqs[:16], max_steps=max(3, args.warmup), **kw)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    t0 = time.perf_counter()
+    steps = run_trace(torch, api, W, reqs, **kw)
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    busy = [st for st in steps if st["T"] > 0]
+    tokens = sum(st["T"] for st in busy)
+    gpu_ms = sum(st["gpu_ms"] for st in busy)
+    roof = [trace_step_roofline(st, cfg["num_layers"], cfg["num_heads"], cfg["head_dim"], peaks)
+            for st in busy]
+    fracs = np.array([r[0] / st["gpu_ms"] for r, st in zip(roof, busy)])
+    sched_us = 1e6 * np.mean([st["sched_s"] for st in steps])
+    line = {"metric": METRIC, "value": tokens / (gpu_ms * 1e-3), "unit": UNIT, "n_gpus": 1,
+            "steps": len(steps), "warmup": max(3, args.warmup), "ms_per_step": gpu_ms / len(busy),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": label, "requests": len(reqs), "layers": cfg["num_layers"],
+                       "tokens_total": tokens, "l2": "inputs larger than L2 (86 GB of KV pools)",
+                       "timed": "cb_append_kv + cb_ragged_attention of every layer of every step; "
+                                "Q/K/V generation between layers not timed"},
+            "step_roofline": {"frac_total": sum(r[0] for r in roof) / gpu_ms,
+                              "frac_p10": float(np.percentile(fracs, 10)),
+                              "frac_p50": float(np.percentile(fracs, 50)),
+                              "frac_p90": float(np.percentile(fracs, 90)),
+                              "bytes_total": sum(r[1] for r in roof), "flops_total": sum(r[2] for r in roof)},
+            "scheduler_us_per_step": sched_us, "wall_s": wall,
+            "mean_decode_per_step": float(np.mean([st["decode"] for st in busy])),
+            "clocks": clocks, "gpu_launches": sum(cfg["num_layers"] * launches_per_layer(st) for st in busy)}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "mixed", "long", "tiny"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "mixed", "long", "tiny", "trace"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 
+    if args.workload == "trace":
+        run_trace_bench(args)
+        return
     b, label = make_workload(args.workload)
     if args.impl == "reference":
         run_reference(args, b, label)

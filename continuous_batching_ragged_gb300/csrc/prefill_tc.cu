@@ -20,12 +20,17 @@
 //   * warp 9 (MMA): one thread issues, per KV tile j and query tile t,
 //     S_t = Q_t K_j^T (fp32 in TMEM) and O_t += P_t V_j (P_t read from TMEM,
 //     V as an N-contiguous B operand).  P_t overwrites the first 64 columns of
-//     S_t, so S_t(j+1) is issued only once P_t V_j has completed.
+//     S_t, so S_t(j+1) is issued only once P_t V_j has completed.  (Issuing
+//     S_t(j+1) directly behind P_t V_j, relying on in-order MMA execution, was
+//     measured slower: 1.44 ms against 1.26 ms on a 2048-row chunk over 30720
+//     cached keys.)
 //   * warps 0-3 / 4-7 (softmax of tile 0 / 1): thread i owns query row i =
 //     TMEM lane i.  It loads its 128 scores, masks keys j > p + i only on the
 //     tiles that cross its warp's diagonal, keeps a running max in the exp2
 //     domain (rescaling O in TMEM only when the max grew by more than 2^8),
-//     writes P as bf16 into TMEM, and at the end normalises O and stores.
+//     forms exp arguments and row sums two at a time with packed f32x2
+//     FMA/add, writes P as bf16 into TMEM, and at the end normalises O and
+//     stores.
 // Every mbarrier wait is bounded; a timeout sets the device error word and
 // the CTA winds down, freeing its TMEM.
 #include <cuda.h>
@@ -78,6 +83,31 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Packed fp32 pairs (Blackwell f32x2 FMA / add): two lanes of work per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -265,33 +295,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       const int kb = j * BN;
       float mt = -INFINITY;
-      if (kb + BN - 1 <= warp_limit) {             // every key of the tile visible to the warp
+      if (kb + BN - 1 > warp_limit) {              // the tile crosses some row's diagonal: mask
 #pragma unroll
-        for (int c = 0; c < BN; ++c) mt = fmaxf(mt, __uint_as_float(sr[c]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const float v = kb + c <= limit ? __uint_as_float(sr[c]) : -INFINITY;
-          sr[c] = __float_as_uint(v);
-          mt = fmaxf(mt, v);
-        }
+        for (int c = 0; c < BN; ++c)
+          if (kb + c > limit) sr[c] = __float_as_uint(-INFINITY);
       }
+#pragma unroll
+      for (int c = 0; c < BN; c += 2) mt = max3(mt, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
       const float m_new = fmaxf(m, mt * sl2);
       const bool resc = m_new > m + 8.0f;         // keep a stale max while exp2 stays <= 2^8
       const float m_use = resc ? m_new : m;
       const float alpha = resc ? ex2(m - m_new) : 1.0f;
-      float rs = 0.f;
+      const uint64_t scale2 = f2_pack(sl2, sl2);
+      const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
+      uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 64; ++c) {               // P packed in place over the scores
-        const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
-        const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
-        rs += p0 + p1;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), scale2, neg_m2),
+                  x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        sum2 = f2_add(sum2, f2_pack(p0, p1));
         sr[c] = pack_bf16x2(p0, p1);
       }
+      float rs0, rs1;
+      f2_unpack(sum2, rs0, rs1);
+      const float rs = rs0 + rs1;
       l = l * alpha + rs;
       m = m_use;
       tc_fence_before();
-      if (j > 0) {                                 // P_t V of tile j-1 done: S_t cols free, O_t stable
+      if (j > 0) {                                 // P_t V of tile j-1 done: O_t stable
         if (!mbar_wait(bar(BAR_O + t), (j - 1) & 1)) {
           ok = false;
           break;

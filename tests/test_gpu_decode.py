@@ -34,11 +34,14 @@ def test_decode_edge_contexts(native_lib, dtype, A, B):
 
 
 def test_decode_step_scaled_down(native_lib):
-    """The decode workload's shape (32 x 128, block 16, permuted pool) with 24 sequences."""
-    from gpu_harness import DeviceStep, assert_tolerance, oracle_packed, to_np
+    """The decode workload's shape (32 x 128, block 16, permuted pool) with 24 sequences;
+    every row checked on 4 of the 32 heads."""
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_rows, to_np
     b = W.decode_step(num_seqs=24, seed=21)
     got = to_np(DeviceStep(b, source="device").run())
-    assert_tolerance(got, oracle_packed(b))
+    heads = [0, 7, 19, 31]
+    exp = np.concatenate([oracle_rows(b, s, heads) for s in range(b.num_seqs)])
+    assert_tolerance(got[:, heads], exp)
 
 
 def test_decode_step_full_size_sampled(native_lib):
