@@ -9,30 +9,32 @@
 // and each block's contribution is accumulated into a running state (online
 // softmax).
 //
-// One CTA computes two 128-row query tiles of one (sequence, head); the two
-// tiles share every K/V tile loaded into shared memory, and each tile's
-// softmax overlaps the other tile's MMAs on the tensor core.
-//   * warp 8 (TMA): loads both Q tiles once, then K and V tiles of 128 keys
-//     into a 2-stage ring; a 128-key tile is 128/B paged blocks, each one 3-D
-//     TMA box [B rows x 64 dims] per 64-dim half, 128-byte swizzled.  Blocks
-//     past the context are requested at an out-of-range coordinate, which TMA
-//     fills with zeros.
-//   * warp 9 (MMA): one thread issues, per KV tile j and query tile t,
-//     S_t = Q_t K_j^T (fp32 in TMEM) and O_t += P_t V_j (P_t read from TMEM,
-//     V as an N-contiguous B operand).  P_t overwrites the first 64 columns of
-//     S_t, so S_t(j+1) is issued only once P_t V_j has completed.  (Issuing
-//     S_t(j+1) directly behind P_t V_j, relying on in-order MMA execution, was
-//     measured slower: 1.44 ms against 1.26 ms on a 2048-row chunk over 30720
-//     cached keys.)
+// One CTA computes two 128-row query tiles of one (sequence, head).  Both
+// tiles share every K/V tile loaded into shared memory, and the tiles run in
+// ping-pong: while one tile's softmax works, the tensor core runs the other
+// tile's MMAs.
+//   * warp 8 (K loader) and warp 10 (V loader): TMA into a 3-stage K ring and
+//     a 2-stage V ring, so a K tile is freed as soon as both S MMAs have read
+//     it and the next S never waits behind a V still in use.  A 128-key tile
+//     is 128/B paged blocks, one 3-D TMA box [B rows x 64 dims] per block and
+//     64-dim half, 128-byte swizzled.  Blocks past the context are requested
+//     at an out-of-range coordinate, which TMA fills with zeros; the rows of
+//     the last, partial block past the context are zeroed by the V loader
+//     (P is 0 there but 0 * NaN is NaN).
+//   * warp 9 (MMA): one thread runs an event loop over both tiles, issuing
+//     whichever MMA is ready: S_t = Q_t K_j^T (fp32 in TMEM) once K_j has
+//     landed and P_t V_{j-1} has completed (P_t overwrites the first 64
+//     columns of S_t), and O_t += P_t V_j (P_t read from TMEM, V as an
+//     N-contiguous B operand) once the softmax has written P_t.
 //   * warps 0-3 / 4-7 (softmax of tile 0 / 1): thread i owns query row i =
 //     TMEM lane i.  It loads its 128 scores, masks keys j > p + i only on the
 //     tiles that cross its warp's diagonal, keeps a running max in the exp2
 //     domain (rescaling O in TMEM only when the max grew by more than 2^8),
 //     forms exp arguments and row sums two at a time with packed f32x2
 //     FMA/add, writes P as bf16 into TMEM, and at the end normalises O and
-//     stores.
-// Every mbarrier wait is bounded; a timeout sets the device error word and
-// the CTA winds down, freeing its TMEM.
+//     stores its row.
+// Every wait is bounded; a timeout sets the device error word and the CTA
+// winds down, freeing its TMEM.
 #include <cuda.h>
 
 #include "device_common.cuh"
@@ -49,26 +51,30 @@ constexpr int BM = 128;                          // query rows per tile = TMEM l
 constexpr int BN = 128;                          // keys per KV tile
 constexpr int HD = 128;                          // head dim
 constexpr int kQTiles = 2;                       // query tiles per CTA
-constexpr int kStages = 2;                       // K/V ring depth
-constexpr int kThreads = 320;                    // warps 0-7 softmax, 8 TMA, 9 MMA
-constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kKStages = 3;                      // K ring depth
+constexpr int kVStages = 2;                      // V ring depth
+constexpr int kThreads = 352;                    // warps 0-7 softmax, 8 K loader, 9 MMA, 10 V loader
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
 constexpr uint32_t kHalf = BM * 64 * 2;          // one 64-dim swizzled half: 16 KB
 constexpr uint32_t kTile = 2 * kHalf;            // a 128 x 128 bf16 tile: 32 KB
 constexpr uint32_t kTmemCols = 512;              // per tile t: S at 256t, O at 256t + 128
+constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQTiles * kTile;
-constexpr uint32_t kOffV = kOffK + kStages * kTile;
-constexpr uint32_t kOffBar = kOffV + kStages * kTile;
+constexpr uint32_t kOffV = kOffK + kKStages * kTile;
+constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
 enum : int {
   BAR_Q = 0,
-  BAR_S = 1,                  // + t
-  BAR_P = BAR_S + kQTiles,    // + t
-  BAR_O = BAR_P + kQTiles,    // + t
-  BAR_KF = BAR_O + kQTiles,   // + stage
-  BAR_VF = BAR_KF + kStages,
-  BAR_KVE = BAR_VF + kStages,
-  NUM_BARS = BAR_KVE + kStages
+  BAR_S = 1,                   // + t: S_t ready
+  BAR_P = BAR_S + kQTiles,     // + t: P_t written (128 arrivals)
+  BAR_O = BAR_P + kQTiles,     // + t: P_t V done
+  BAR_KF = BAR_O + kQTiles,    // + stage: K landed
+  BAR_KE = BAR_KF + kKStages,  // + stage: K consumed
+  BAR_VF = BAR_KE + kKStages,  // + stage: V landed (and its tail zeroed)
+  BAR_VE = BAR_VF + kVStages,  // + stage: V consumed
+  BAR_VTAIL = BAR_VE + kVStages,
+  NUM_BARS = BAR_VTAIL + 1
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + 8 * NUM_BARS;
 constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;   // + slack to align the base to 1 KB
@@ -110,6 +116,32 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
+// Physical box index (block * H + head) of each paged block of KV tile j, or
+// `oob` (zero fill) for blocks past the context.
+__device__ __forceinline__ void tile_boxes(int j, int B, int ctx, const int32_t* bt, const AttnArgs& a,
+                                           int h, int (&z)[16]) {
+  const int bpt = BN / B;
+  const int oob = a.num_blocks * a.num_heads;
+  for (int bi = 0; bi < bpt; ++bi) {
+    const int lb = j * bpt + bi;
+    z[bi] = oob;
+    if (lb * B < ctx) {
+      const int blk = bt[lb];
+      if (blk >= 0 && blk < a.num_blocks) z[bi] = blk * a.num_heads + h;
+      else raise_error(a.err, kErrBounds);
+    }
+  }
+}
+
+__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int B,
+                                             const int (&z)[16]) {
+  const int bpt = BN / B;
+  for (int bi = 0; bi < bpt; ++bi) {
+    tma_load_3d(dst + bi * B * 128, tm, bar, 0, 0, z[bi]);
+    tma_load_3d(dst + kHalf + bi * B * 128, tm, bar, 64, 0, z[bi]);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
@@ -142,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return base + kOffBar + 8u * uint32_t(i); };
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int32_t* bt = a.block_tables + size_t(s) * a.max_blocks_per_seq;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
@@ -150,11 +183,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(BAR_P + t), BM);
       mbar_init(bar(BAR_O + t), 1);
     }
-    for (int st = 0; st < kStages; ++st) {
+    for (int st = 0; st < kKStages; ++st) {
       mbar_init(bar(BAR_KF + st), 1);
-      mbar_init(bar(BAR_VF + st), 1);
-      mbar_init(bar(BAR_KVE + st), 1);
+      mbar_init(bar(BAR_KE + st), 1);
     }
+    for (int st = 0; st < kVStages; ++st) {
+      mbar_init(bar(BAR_VF + st), 1);
+      mbar_init(bar(BAR_VE + st), 1);
+    }
+    mbar_init(bar(BAR_VTAIL), 1);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -165,109 +202,126 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gsm + kOffTmemSlot);
 
-  if (warp == kWarpTma) {
-    // ---------------------------------------------------------------- TMA
+  if (warp == kWarpK) {
+    // ------------------------------------------------------------ K loader
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(bar(BAR_Q), kQTiles * kTile);
       for (int t = 0; t < kQTiles; ++t) {
         tma_load_3d(base + kOffQ + t * kTile, &tm_q, bar(BAR_Q), 0, h, c0 + row0 + t * BM);
         tma_load_3d(base + kOffQ + t * kTile + kHalf, &tm_q, bar(BAR_Q), 64, h, c0 + row0 + t * BM);
       }
-      const int bpt = BN / B;                      // paged blocks per KV tile
-      const int32_t* bt = a.block_tables + size_t(s) * a.max_blocks_per_seq;
-      const int oob = a.num_blocks * a.num_heads;  // first out-of-range box index: zero fill
       int z[16];
       for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages && !mbar_wait(bar(BAR_KVE + st), ((j / kStages) - 1) & 1)) {
+        const int st = j % kKStages;
+        if (j >= kKStages && !mbar_wait(bar(BAR_KE + st), ((j / kKStages) - 1) & 1)) {
           raise_error(a.err, kErrTimeout);
           break;
         }
-        for (int bi = 0; bi < bpt; ++bi) {
-          const int lb = j * bpt + bi;
-          z[bi] = oob;
-          if (lb * B < ctx) {
-            const int blk = bt[lb];
-            if (blk >= 0 && blk < a.num_blocks) z[bi] = blk * a.num_heads + h;
-            else raise_error(a.err, kErrBounds);
-          }
-        }
-        const uint32_t kdst = base + kOffK + st * kTile;
-        const uint32_t vdst = base + kOffV + st * kTile;
+        tile_boxes(j, B, ctx, bt, a, h, z);
         mbar_arrive_expect_tx(bar(BAR_KF + st), kTile);
-        for (int bi = 0; bi < bpt; ++bi) {
-          tma_load_3d(kdst + bi * B * 128, &tm_k, bar(BAR_KF + st), 0, 0, z[bi]);
-          tma_load_3d(kdst + kHalf + bi * B * 128, &tm_k, bar(BAR_KF + st), 64, 0, z[bi]);
+        load_kv_tile(base + kOffK + st * kTile, &tm_k, bar(BAR_KF + st), B, z);
+      }
+    }
+  } else if (warp == kWarpV) {
+    // ------------------------------------------------------------ V loader
+    if (lane == 0) tma_prefetch_desc(&tm_v);
+    int z[16];
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j % kVStages;
+      if (j >= kVStages && !mbar_wait(bar(BAR_VE + st), ((j / kVStages) - 1) & 1)) {
+        if (lane == 0) raise_error(a.err, kErrTimeout);
+        break;
+      }
+      const int kb = j * BN;
+      const int r0 = ctx - kb;                               // first row past the context
+      const int r1 = min(BN, ((ctx + B - 1) / B) * B - kb);  // end of the last paged block
+      const bool tail = j == n_tiles - 1 && r0 < r1;
+      const uint32_t vdst = base + kOffV + st * kTile;
+      if (lane == 0) {
+        tile_boxes(j, B, ctx, bt, a, h, z);
+        const uint32_t land = tail ? bar(BAR_VTAIL) : bar(BAR_VF + st);
+        mbar_arrive_expect_tx(land, kTile);
+        load_kv_tile(vdst, &tm_v, land, B, z);
+      }
+      if (tail) {
+        // zero the stale rows of the last paged block, then publish the tile
+        if (!mbar_wait(bar(BAR_VTAIL), 0)) {
+          if (lane == 0) raise_error(a.err, kErrTimeout);
+          break;
         }
-        mbar_arrive_expect_tx(bar(BAR_VF + st), kTile);
-        for (int bi = 0; bi < bpt; ++bi) {
-          tma_load_3d(vdst + bi * B * 128, &tm_v, bar(BAR_VF + st), 0, 0, z[bi]);
-          tma_load_3d(vdst + kHalf + bi * B * 128, &tm_v, bar(BAR_VF + st), 64, 0, z[bi]);
+        uint8_t* vt = gsm + kOffV + st * kTile;
+        for (int c = lane; c < (r1 - r0) * 16; c += 32) {
+          const int r = r0 + c / 16, w = c % 16;
+          *reinterpret_cast<uint4*>(vt + (w / 8) * kHalf + r * 128 + (w % 8) * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_VF + st));
       }
     }
   } else if (warp == kWarpMma) {
-    // ---------------------------------------------------------------- MMA
+    // ------------------------------------------------------------ MMA
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);   // Q (K-major) x K (K-major)
       constexpr uint32_t idO = idesc_bf16_f32(BM, HD, true);    // P (TMEM) x V (N-contiguous)
-      auto issue_s = [&](int t, int j) {
-        const uint32_t kb = base + kOffK + (j % kStages) * kTile;
-        const uint32_t qb = base + kOffQ + t * kTile;
+      // js[t]: next KV tile whose S_t is to be issued; jp[t]: next P_t V to issue.
+      int js[kQTiles] = {0, 0}, jp[kQTiles] = {0, n_tiles};
+      if (nq == 2) jp[1] = 0;
+      else js[1] = n_tiles;                        // tile 1 idle: never issued, never waited on
+      bool ok = mbar_wait(bar(BAR_Q), 0);
+      uint64_t last = globaltimer_ns();
+      uint32_t spins = 0;
+      while (ok && (jp[0] < n_tiles || jp[1] < n_tiles)) {
+        bool progressed = false;
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
-          mma_f16_ss(tmem + 256 * t, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS,
-                     k > 0);
-        }
-        mma_commit(bar(BAR_S + t));
-      };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t vb = base + kOffV + (j % kStages) * kTile;
+        for (int t = 0; t < kQTiles; ++t) {
+          // S_t(x): K_x landed and P_t V_{x-1} complete (its P sits in S_t's columns)
+          if (js[t] < n_tiles && js[t] == jp[t]) {
+            const int x = js[t];
+            if ((x == 0 || mbar_try_wait(bar(BAR_O + t), (x - 1) & 1)) &&
+                mbar_try_wait(bar(BAR_KF + x % kKStages), (x / kKStages) & 1)) {
+              tc_fence_after();
+              const uint32_t kb = base + kOffK + (x % kKStages) * kTile;
+              const uint32_t qb = base + kOffQ + t * kTile;
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          mma_f16_ts(tmem + 256 * t + 128, tmem + 256 * t + k * 8, smem_desc(vb + k * 2048, kHalf, 1024),
-                     idO, (j > 0 || k > 0));
-        mma_commit(bar(BAR_O + t));
-      };
-      bool ok = mbar_wait(bar(BAR_Q), 0) && mbar_wait(bar(BAR_KF), 0);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < nq; ++t) issue_s(t, 0);
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % kStages;
-        if (!mbar_wait(bar(BAR_VF + st), (j / kStages) & 1)) {
-          ok = false;
-          break;
-        }
-        for (int t = 0; t < nq; ++t) {
-          if (!mbar_wait(bar(BAR_P + t), j & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_pv(t, j);
-        }
-        if (!ok) break;
-        mma_commit(bar(BAR_KVE + st));
-        if (j + 1 < n_tiles) {
-          if (!mbar_wait(bar(BAR_KF + (j + 1) % kStages), ((j + 1) / kStages) & 1)) {
-            ok = false;
-            break;
-          }
-          for (int t = 0; t < nq; ++t) {
-            // P_t lives in S_t's columns: wait for P_t V_j before overwriting them
-            if (!mbar_wait(bar(BAR_O + t), j & 1)) {
-              ok = false;
-              break;
+              for (int k = 0; k < HD / 16; ++k) {
+                const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
+                mma_f16_ss(tmem + 256 * t, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024),
+                           idS, k > 0);
+              }
+              mma_commit(bar(BAR_S + t));
+              js[t] = x + 1;
+              if (min(js[0], js[1]) > x) mma_commit(bar(BAR_KE + x % kKStages));   // both read K_x
+              progressed = true;
             }
-            tc_fence_after();
-            issue_s(t, j + 1);
           }
+          // O_t += P_t(x) V_x: the softmax wrote P_t(x) and V_x landed
+          if (jp[t] < js[t]) {
+            const int x = jp[t];
+            if (mbar_try_wait(bar(BAR_P + t), x & 1) &&
+                mbar_try_wait(bar(BAR_VF + x % kVStages), (x / kVStages) & 1)) {
+              tc_fence_after();
+              const uint32_t vb = base + kOffV + (x % kVStages) * kTile;
+#pragma unroll
+              for (int k = 0; k < BN / 16; ++k)
+                mma_f16_ts(tmem + 256 * t + 128, tmem + 256 * t + k * 8,
+                           smem_desc(vb + k * 2048, kHalf, 1024), idO, (x > 0 || k > 0));
+              mma_commit(bar(BAR_O + t));
+              jp[t] = x + 1;
+              if (min(jp[0], jp[1]) > x) mma_commit(bar(BAR_VE + x % kVStages));   // both read V_x
+              progressed = true;
+            }
+          }
+        }
+        if (progressed) {
+          spins = 0;
+          last = 0;
+        } else if ((++spins & 63u) == 0) {
+          const uint64_t now = globaltimer_ns();
+          if (last == 0) last = now;
+          else if (now - last > kTimeoutNs) ok = false;
         }
       }
       if (!ok) raise_error(a.err, kErrTimeout);
@@ -345,28 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       tmem_st32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_st();
-      if (t == 0 && j == n_tiles - 1) {
-        // Rows of the last paged block past the context hold stale cache bytes;
-        // P is 0 there but 0 * NaN is NaN, so zero those V rows (whole blocks
-        // past the context already arrived as TMA zero fill).  Tile 0's P V is
-        // issued first, so this also covers tile 1.
-        const int r0 = ctx - kb;
-        const int r1 = min(BN, ((ctx + B - 1) / B) * B - kb);
-        if (r0 < r1) {
-          const int st = j % kStages;
-          if (!mbar_wait(bar(BAR_VF + st), (j / kStages) & 1)) {
-            ok = false;
-            break;
-          }
-          uint8_t* vt = gsm + kOffV + st * kTile;
-          const int chunks = (r1 - r0) * 16;       // 16-byte chunks over both halves
-          for (int c = i; c < chunks; c += BM) {
-            const int r = r0 + c / 16, w = c % 16;
-            *reinterpret_cast<uint4*>(vt + (w / 8) * kHalf + r * 128 + (w % 8) * 16) = make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-        }
-      }
       tc_fence_before();
       mbar_arrive(bar(BAR_P + t));
     }
