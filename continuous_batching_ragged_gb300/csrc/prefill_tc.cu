@@ -15,17 +15,22 @@
 // tile's MMAs.
 //   * warp 8 (K loader) and warp 10 (V loader): TMA into a 3-stage K ring and
 //     a 2-stage V ring, so a K tile is freed as soon as both S MMAs have read
-//     it and the next S never waits behind a V still in use.  A 128-key tile
+//     it and the next S never waits behind a V still in use.  Each loader
+//     looks up the block table four tiles ahead (one coalesced load per tile
+//     into a small shared ring) and asks TMA to prefetch those boxes into L2,
+//     so a stage is refilled the moment it frees and the load hits L2.  A 128-key tile
 //     is 128/B paged blocks, one 3-D TMA box [B rows x 64 dims] per block and
 //     64-dim half, 128-byte swizzled.  Blocks past the context are requested
 //     at an out-of-range coordinate, which TMA fills with zeros; the rows of
 //     the last, partial block past the context are zeroed by the V loader
 //     (P is 0 there but 0 * NaN is NaN).
-//   * warp 9 (MMA): one thread runs an event loop over both tiles, issuing
-//     whichever MMA is ready: S_t = Q_t K_j^T (fp32 in TMEM) once K_j has
-//     landed and P_t V_{j-1} has completed (P_t overwrites the first 64
-//     columns of S_t), and O_t += P_t V_j (P_t read from TMEM, V as an
-//     N-contiguous B operand) once the softmax has written P_t.
+//   * warp 9 (MMA): one thread issues, per KV tile j, P_0 V_j, S_0(j+1),
+//     P_1 V_j, S_1(j+1): S_t = Q_t K^T in fp32 TMEM (K-major SS descriptors),
+//     O_t += P_t V with P_t (bf16) read from TMEM and V an N-contiguous B
+//     operand.  P_t overwrites the first 64 columns of S_t; S_t(j+1) comes
+//     right behind P_t V_j, which the in-order execution of one thread's
+//     tcgen05.mma ops keeps safe.  Each tile's softmax thus overlaps the
+//     other tile's two MMA groups.
 //   * warps 0-3 / 4-7 (softmax of tile 0 / 1): thread i owns query row i =
 //     TMEM lane i.  It loads its 128 scores, masks keys j > p + i only on the
 //     tiles that cross its warp's diagonal, keeps a running max in the exp2
@@ -58,7 +63,6 @@ constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
 constexpr uint32_t kHalf = BM * 64 * 2;          // one 64-dim swizzled half: 16 KB
 constexpr uint32_t kTile = 2 * kHalf;            // a 128 x 128 bf16 tile: 32 KB
 constexpr uint32_t kTmemCols = 512;              // per tile t: S at 256t, O at 256t + 128
-constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQTiles * kTile;
@@ -77,7 +81,11 @@ enum : int {
   NUM_BARS = BAR_VTAIL + 1
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + 8 * NUM_BARS;
-constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;   // + slack to align the base to 1 KB
+constexpr int kLookAhead = 4;                    // tiles of block-table look-ahead and L2 prefetch
+constexpr int kRing = 8;                         // box-index ring slots per loader (> kLookAhead)
+constexpr uint32_t kOffRing = kOffTmemSlot + 16; // two rings (K, V) of kRing x 16 ints
+constexpr uint32_t kSmemBytes = kOffRing + 2 * kRing * 16 * 4 + 1024;   // + slack to align the base
+static_assert(kRing > kLookAhead, "ring must outlive the look-ahead");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
@@ -116,29 +124,42 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
-// Physical box index (block * H + head) of each paged block of KV tile j, or
-// `oob` (zero fill) for blocks past the context.
-__device__ __forceinline__ void tile_boxes(int j, int B, int ctx, const int32_t* bt, const AttnArgs& a,
-                                           int h, int (&z)[16]) {
-  const int bpt = BN / B;
-  const int oob = a.num_blocks * a.num_heads;
-  for (int bi = 0; bi < bpt; ++bi) {
-    const int lb = j * bpt + bi;
-    z[bi] = oob;
-    if (lb * B < ctx) {
-      const int blk = bt[lb];
-      if (blk >= 0 && blk < a.num_blocks) z[bi] = blk * a.num_heads + h;
-      else raise_error(a.err, kErrBounds);
-    }
-  }
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z)
+               : "memory");
 }
 
-__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int B,
-                                             const int (&z)[16]) {
+// Warp-wide: lane i < 128/B looks up paged block i of KV tile j in one coalesced
+// load, stores its box index (or `oob`, zero fill) in the ring slot of tile j,
+// and asks TMA to prefetch that box into L2 for the load a few tiles later.
+__device__ __forceinline__ void stage_boxes(int j, int B, int ctx, const int32_t* bt, const AttnArgs& a,
+                                            int h, int lane, int* ring, const CUtensorMap* tm) {
+  const int bpt = BN / B;
+  if (lane < bpt) {
+    const int lb = j * bpt + lane;
+    int z = a.num_blocks * a.num_heads;
+    if (lb * B < ctx) {
+      const int blk = bt[lb];
+      if (blk >= 0 && blk < a.num_blocks) {
+        z = blk * a.num_heads + h;
+        tma_prefetch_l2_3d(tm, 0, 0, z);
+        tma_prefetch_l2_3d(tm, 64, 0, z);
+      } else {
+        raise_error(a.err, kErrBounds);
+      }
+    }
+    ring[(j % kRing) * 16 + lane] = z;
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void load_kv_tile_ring(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int B,
+                                                  const int* zs) {
   const int bpt = BN / B;
   for (int bi = 0; bi < bpt; ++bi) {
-    tma_load_3d(dst + bi * B * 128, tm, bar, 0, 0, z[bi]);
-    tma_load_3d(dst + kHalf + bi * B * 128, tm, bar, 64, 0, z[bi]);
+    tma_load_3d(dst + bi * B * 128, tm, bar, 0, 0, zs[bi]);
+    tma_load_3d(dst + kHalf + bi * B * 128, tm, bar, 64, 0, zs[bi]);
   }
 }
 
@@ -204,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpK) {
     // ------------------------------------------------------------ K loader
+    int* ring = reinterpret_cast<int*>(gsm + kOffRing);
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -212,25 +234,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(base + kOffQ + t * kTile, &tm_q, bar(BAR_Q), 0, h, c0 + row0 + t * BM);
         tma_load_3d(base + kOffQ + t * kTile + kHalf, &tm_q, bar(BAR_Q), 64, h, c0 + row0 + t * BM);
       }
-      int z[16];
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % kKStages;
-        if (j >= kKStages && !mbar_wait(bar(BAR_KE + st), ((j / kKStages) - 1) & 1)) {
-          raise_error(a.err, kErrTimeout);
-          break;
-        }
-        tile_boxes(j, B, ctx, bt, a, h, z);
-        mbar_arrive_expect_tx(bar(BAR_KF + st), kTile);
-        load_kv_tile(base + kOffK + st * kTile, &tm_k, bar(BAR_KF + st), B, z);
+    }
+    for (int j = 0; j < min(kLookAhead, n_tiles); ++j) stage_boxes(j, B, ctx, bt, a, h, lane, ring, &tm_k);
+    for (int j = 0; j < n_tiles; ++j) {
+      if (j + kLookAhead < n_tiles) stage_boxes(j + kLookAhead, B, ctx, bt, a, h, lane, ring, &tm_k);
+      const int st = j % kKStages;
+      if (j >= kKStages && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_KE + st), ((j / kKStages) - 1) & 1))) {
+        if (lane == 0) raise_error(a.err, kErrTimeout);
+        break;
       }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(BAR_KF + st), kTile);
+        load_kv_tile_ring(base + kOffK + st * kTile, &tm_k, bar(BAR_KF + st), B, ring + (j % kRing) * 16);
+      }
+      __syncwarp();
     }
   } else if (warp == kWarpV) {
     // ------------------------------------------------------------ V loader
+    int* ring = reinterpret_cast<int*>(gsm + kOffRing) + kRing * 16;
     if (lane == 0) tma_prefetch_desc(&tm_v);
-    int z[16];
+    for (int j = 0; j < min(kLookAhead, n_tiles); ++j) stage_boxes(j, B, ctx, bt, a, h, lane, ring, &tm_v);
     for (int j = 0; j < n_tiles; ++j) {
+      if (j + kLookAhead < n_tiles) stage_boxes(j + kLookAhead, B, ctx, bt, a, h, lane, ring, &tm_v);
       const int st = j % kVStages;
-      if (j >= kVStages && !mbar_wait(bar(BAR_VE + st), ((j / kVStages) - 1) & 1)) {
+      if (j >= kVStages && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_VE + st), ((j / kVStages) - 1) & 1))) {
         if (lane == 0) raise_error(a.err, kErrTimeout);
         break;
       }
@@ -240,14 +267,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool tail = j == n_tiles - 1 && r0 < r1;
       const uint32_t vdst = base + kOffV + st * kTile;
       if (lane == 0) {
-        tile_boxes(j, B, ctx, bt, a, h, z);
         const uint32_t land = tail ? bar(BAR_VTAIL) : bar(BAR_VF + st);
         mbar_arrive_expect_tx(land, kTile);
-        load_kv_tile(vdst, &tm_v, land, B, z);
+        load_kv_tile_ring(vdst, &tm_v, land, B, ring + (j % kRing) * 16);
       }
+      __syncwarp();
       if (tail) {
         // zero the stale rows of the last paged block, then publish the tile
-        if (!mbar_wait(bar(BAR_VTAIL), 0)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_VTAIL), 0))) {
           if (lane == 0) raise_error(a.err, kErrTimeout);
           break;
         }
@@ -266,62 +293,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);   // Q (K-major) x K (K-major)
       constexpr uint32_t idO = idesc_bf16_f32(BM, HD, true);    // P (TMEM) x V (N-contiguous)
-      // js[t]: next KV tile whose S_t is to be issued; jp[t]: next P_t V to issue.
-      int js[kQTiles] = {0, 0}, jp[kQTiles] = {0, n_tiles};
-      if (nq == 2) jp[1] = 0;
-      else js[1] = n_tiles;                        // tile 1 idle: never issued, never waited on
-      bool ok = mbar_wait(bar(BAR_Q), 0);
-      uint64_t last = globaltimer_ns();
-      uint32_t spins = 0;
-      while (ok && (jp[0] < n_tiles || jp[1] < n_tiles)) {
-        bool progressed = false;
+      auto issue_s = [&](int t, int x) {
+        const uint32_t kb = base + kOffK + (x % kKStages) * kTile;
+        const uint32_t qb = base + kOffQ + t * kTile;
 #pragma unroll
-        for (int t = 0; t < kQTiles; ++t) {
-          // S_t(x): K_x landed and P_t V_{x-1} complete (its P sits in S_t's columns)
-          if (js[t] < n_tiles && js[t] == jp[t]) {
-            const int x = js[t];
-            if ((x == 0 || mbar_try_wait(bar(BAR_O + t), (x - 1) & 1)) &&
-                mbar_try_wait(bar(BAR_KF + x % kKStages), (x / kKStages) & 1)) {
-              tc_fence_after();
-              const uint32_t kb = base + kOffK + (x % kKStages) * kTile;
-              const uint32_t qb = base + kOffQ + t * kTile;
-#pragma unroll
-              for (int k = 0; k < HD / 16; ++k) {
-                const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
-                mma_f16_ss(tmem + 256 * t, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024),
-                           idS, k > 0);
-              }
-              mma_commit(bar(BAR_S + t));
-              js[t] = x + 1;
-              if (min(js[0], js[1]) > x) mma_commit(bar(BAR_KE + x % kKStages));   // both read K_x
-              progressed = true;
-            }
-          }
-          // O_t += P_t(x) V_x: the softmax wrote P_t(x) and V_x landed
-          if (jp[t] < js[t]) {
-            const int x = jp[t];
-            if (mbar_try_wait(bar(BAR_P + t), x & 1) &&
-                mbar_try_wait(bar(BAR_VF + x % kVStages), (x / kVStages) & 1)) {
-              tc_fence_after();
-              const uint32_t vb = base + kOffV + (x % kVStages) * kTile;
-#pragma unroll
-              for (int k = 0; k < BN / 16; ++k)
-                mma_f16_ts(tmem + 256 * t + 128, tmem + 256 * t + k * 8,
-                           smem_desc(vb + k * 2048, kHalf, 1024), idO, (x > 0 || k > 0));
-              mma_commit(bar(BAR_O + t));
-              jp[t] = x + 1;
-              if (min(jp[0], jp[1]) > x) mma_commit(bar(BAR_VE + x % kVStages));   // both read V_x
-              progressed = true;
-            }
-          }
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
+          mma_f16_ss(tmem + 256 * t, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, k > 0);
         }
-        if (progressed) {
-          spins = 0;
-          last = 0;
-        } else if ((++spins & 63u) == 0) {
-          const uint64_t now = globaltimer_ns();
-          if (last == 0) last = now;
-          else if (now - last > kTimeoutNs) ok = false;
+        mma_commit(bar(BAR_S + t));
+      };
+      auto issue_pv = [&](int t, int x) {
+        const uint32_t vb = base + kOffV + (x % kVStages) * kTile;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          mma_f16_ts(tmem + 256 * t + 128, tmem + 256 * t + k * 8, smem_desc(vb + k * 2048, kHalf, 1024), idO,
+                     (x > 0 || k > 0));
+        mma_commit(bar(BAR_O + t));
+      };
+      // Fixed issue order per KV tile j: P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1).
+      // S_t(j+1) overwrites the TMEM columns that P_t V_j reads; tcgen05.mma
+      // ops issued by one thread execute in issue order, so the read comes
+      // first.  While the softmax of one tile runs, the tensor core works
+      // through the other tile's P V and next S.
+      bool ok = mbar_wait(bar(BAR_Q), 0) && mbar_wait(bar(BAR_KF), 0);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < nq; ++t) issue_s(t, 0);
+        mma_commit(bar(BAR_KE));
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const bool next = j + 1 < n_tiles;
+        if (!mbar_wait(bar(BAR_VF + j % kVStages), (j / kVStages) & 1)) {
+          ok = false;
+          break;
+        }
+        for (int t = 0; t < nq; ++t) {
+          if (!mbar_wait(bar(BAR_P + t), j & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, j);
+          if (t == nq - 1) mma_commit(bar(BAR_VE + j % kVStages));          // both read V_j
+          if (next) {
+            if (t == 0 && !mbar_wait(bar(BAR_KF + (j + 1) % kKStages), ((j + 1) / kKStages) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, j + 1);
+            if (t == nq - 1) mma_commit(bar(BAR_KE + (j + 1) % kKStages));  // both read K_{j+1}
+          }
         }
       }
       if (!ok) raise_error(a.err, kErrTimeout);
