@@ -39,10 +39,10 @@ NOMINAL_HBM_GBS = 8000.0
 # workloads
 # ---------------------------------------------------------------------------
 
-def make_workload(name: str):
+def make_workload(name: str, decode_seqs: int = 256):
     from continuous_batching_ragged_gb300 import workloads as W
     if name == "decode":
-        return W.decode_step(), "decode_256seq_ctx512-4096_bf16_H32_A128_B16"
+        return W.decode_step(num_seqs=decode_seqs), f"decode_{decode_seqs}seq_ctx512-4096_bf16_H32_A128_B16"
     if name == "mixed":
         return W.mixed_step(), "mixed_m2048_64decode_ctx256-4096_chunks661-661-662_bf16_H32_A128_B16"
     if name == "long":
@@ -439,6 +439,8 @@ def main():
     ap.add_argument("--workload", default="decode", choices=["decode", "mixed", "long", "tiny", "trace"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-seqs", type=int, default=256,
+                    help="sequences of the decode workload (smaller cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -446,7 +448,7 @@ def main():
     if args.workload == "trace":
         run_trace_bench(args)
         return
-    b, label = make_workload(args.workload)
+    b, label = make_workload(args.workload, args.decode_seqs)
     if args.impl == "reference":
         run_reference(args, b, label)
         return
