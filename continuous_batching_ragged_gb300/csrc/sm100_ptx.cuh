@@ -89,6 +89,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// Contiguous bulk copy global -> shared (both 16-byte aligned, size a multiple
+// of 16) completing `bytes` of transaction count on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (tensor cores, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -11,9 +11,13 @@
 // goal is bytes in flight, not arithmetic:
 //   * grid (split, head, row): a row's keys are cut into fixed 512-key splits,
 //     so a long context spreads over many CTAs;
-//   * 4 warps per CTA, each warp walks 16-key tiles; a lane issues 16-byte
-//     loads, half a warp covers one 256-byte key row, so each load instruction
-//     of the warp reads two whole rows of one paged (block, head) tile;
+//   * 4 warps per CTA, each warp walks 16-key tiles; a lane handles one
+//     16-byte chunk of a key row, half a warp covers one 256-byte row;
+//   * bf16, head_dim 128, block size a multiple of 16 (the decode workload):
+//     a 16-key tile of one head is one contiguous 4 KB chunk of the paged pool
+//     for K and one for V, so each warp streams its tiles with 1-D bulk async
+//     copies (cp.async.bulk) into a private 3-stage shared-memory ring, three
+//     tiles ahead of its arithmetic; other shapes load straight to registers;
 //   * the 16-lane dot-product reduction is a transpose-reduce (each shuffle
 //     step halves the rows a lane holds), 8 shuffles for 8 rows instead of 32;
 //   * running max / sum / accumulator per warp, merged across warps in shared
@@ -24,12 +28,15 @@
 #include "device_common.cuh"
 #include "kernels.h"
 #include "runtime.h"
+#include "sm100_ptx.cuh"
 
 namespace cb {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kTile = 16;   // keys per warp iteration
+constexpr int kTile = 16;     // keys per warp iteration
+constexpr int kStages = 3;    // bulk-copy ring depth per warp
+constexpr uint32_t kTileBytes = kTile * 128 * 2;   // one bf16 16 x 128 K (or V) tile: 4 KB
 
 struct SplitArgs {
   AttnArgs a;
@@ -74,22 +81,14 @@ __device__ __forceinline__ void transpose_reduce(float (&v)[N], int lane) {
   }
 }
 
-template <typename T, int A, bool ROW_MODE>
-__global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs sa) {
-  constexpr int EPV = Vec16<T>::N;        // elements per 16-byte load
-  constexpr int LPR = A / EPV;            // lanes per key row
-  constexpr int RPL = 32 / LPR;           // key rows per warp load
-  constexpr int NR = kTile / RPL;         // key rows per lane per tile
-  static_assert(NR <= LPR && NR >= 1, "tile shape");
-  const AttnArgs& a = sa.a;
+// Which query row this CTA serves and which of its keys [k0, k1).
+struct RowPlan {
+  int s, t, nsplit, k0, k1;
+};
 
-  const int split = blockIdx.x;
-  const int h = blockIdx.y;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-
-  // ---- which query row, how many keys ------------------------------------
-  int s, t, key_end;
+template <bool ROW_MODE>
+__device__ __forceinline__ bool plan_row(const AttnArgs& a, int split, int h, RowPlan& pl) {
+  int s, t;
   if (ROW_MODE) {
     t = blockIdx.z;
     int lo = 0, hi = a.num_seqs - 1;
@@ -106,7 +105,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs s
   const int q_len = c1 - c0;
   const int ctx = a.context_lens[s];
   if (!ROW_MODE) {
-    if (q_len > 1) return;                // prefill chunk: not ours
+    if (q_len > 1) return false;          // prefill chunk: not ours
     t = c0;
   }
   const bool bad = q_len < 1 || ctx < q_len || ctx > a.max_context_len || q_len > a.max_q_len ||
@@ -114,41 +113,182 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs s
                    (ctx + a.block_size - 1) / a.block_size > a.max_blocks_per_seq;
   if (bad) {
     if (split == 0 && h == 0 && threadIdx.x == 0) raise_error(a.err, kErrInvalid);
+    return false;
+  }
+  const int key_end = ROW_MODE ? ctx - q_len + (t - c0) + 1 : ctx;
+  pl.s = s;
+  pl.t = t;
+  pl.nsplit = (key_end + kSplitKeys - 1) / kSplitKeys;
+  if (split >= pl.nsplit) return false;
+  pl.k0 = split * kSplitKeys;
+  pl.k1 = min(key_end, pl.k0 + kSplitKeys);
+  return true;
+}
+
+// Shared scratch of the split epilogue.
+template <int A>
+struct MergeSmem {
+  float acc[kWarps][A];
+  float m[kWarps], l[kWarps];
+  int last;
+};
+
+// Combine the warps' (m, l, acc) of this split, then either write the output
+// row (one split) or publish the partial and, in the last CTA of the row to
+// finish, merge all partials by log-sum-exp.
+template <typename T, int A, bool ROW_MODE, int EPV, int LPR>
+__device__ __forceinline__ void finish_split(const SplitArgs& sa, const RowPlan& pl, int split, int h,
+                                             float m_run, float l_run, float (&acc)[EPV],
+                                             MergeSmem<A>& sm) {
+  const AttnArgs& a = sa.a;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane / LPR, c = lane % LPR;
+  // lanes of different row groups hold the same chunk: add them
+#pragma unroll
+  for (int o = LPR; o < 32; o <<= 1) {
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+  }
+  if (g == 0) {
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) sm.acc[warp][c * EPV + e] = acc[e];
+  }
+  if (lane == 0) {
+    sm.m[warp] = m_run;
+    sm.l[warp] = l_run;
+  }
+  __syncthreads();
+
+  const int d = threadIdx.x;
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.m[w]);
+  float L = 0.f, o = 0.f;
+  if (d < A) {
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = ex2(sm.m[w] - M);   // a warp with no keys has m = -inf: weight 0
+      L = fmaf(sm.l[w], f, L);
+      o = fmaf(sm.acc[w][d], f, o);
+    }
+  }
+  T* out_row = static_cast<T*>(a.out) + (size_t(pl.t) * a.num_heads + h) * A;
+  if (pl.nsplit == 1) {
+    if (d < A) store1(out_row + d, o / L);
     return;
   }
-  key_end = ROW_MODE ? ctx - q_len + (t - c0) + 1 : ctx;
-  const int nsplit = (key_end + kSplitKeys - 1) / kSplitKeys;
-  if (split >= nsplit) return;
-  const int k0 = split * kSplitKeys;
-  const int k1 = min(key_end, k0 + kSplitKeys);
-
-  const int g = lane / LPR;               // which key row of a load this lane covers
-  const int c = lane % LPR;               // which 16-byte chunk of the row
-
-  // q row, pre-scaled by scale * log2(e) so scores are in the exp2 domain
-  float qf[EPV];
-  {
-    const uint4 qv = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) +
-                                                     (size_t(t) * a.num_heads + h) * A + c * EPV);
-    Vec16<T>::to_float(qv, qf);
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) qf[e] *= a.scale_log2;
+  const int row_id = ROW_MODE ? pl.t : pl.s;
+  float* part = sa.partials + ((size_t(row_id) * a.num_heads + h) * sa.max_splits) * (A + 2);
+  if (d < A) part[size_t(split) * (A + 2) + d] = o;
+  if (d == 0) {
+    part[size_t(split) * (A + 2) + A] = M;
+    part[size_t(split) * (A + 2) + A + 1] = L;
   }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t* ticket = sa.tickets + size_t(row_id) * a.num_heads + h;
+    sm.last = atomicAdd(ticket, 1) == pl.nsplit - 1;
+    if (sm.last) *ticket = 0;             // every split has arrived: reset for the next call
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();
+  if (d < A) {
+    float MM = -INFINITY;
+    for (int k = 0; k < pl.nsplit; ++k) MM = fmaxf(MM, __ldcg(part + size_t(k) * (A + 2) + A));
+    float LL = 0.f, oo = 0.f;
+    for (int k = 0; k < pl.nsplit; ++k) {
+      const float* pk = part + size_t(k) * (A + 2);
+      const float f = ex2(__ldcg(pk + A) - MM);
+      LL = fmaf(__ldcg(pk + A + 1), f, LL);
+      oo = fmaf(__ldcg(pk + d), f, oo);
+    }
+    store1(out_row + d, oo / LL);
+  }
+}
+
+// One 16-key tile of the online softmax: scores of the lane's NR rows from
+// kv[], running max/sum update, accumulate p * v into acc.
+template <typename T, int EPV, int LPR, int RPL, int NR>
+__device__ __forceinline__ void tile_update(const float (&qf)[EPV], const uint4 (&kv)[NR], const uint4 (&vv)[NR],
+                                            int base, int k1, int lane, float& m_run, float& l_run,
+                                            float (&acc)[EPV]) {
+  const int g = lane / LPR, c = lane % LPR;
+  float sc[NR];
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    float kf[EPV];
+    Vec16<T>::to_float(kv[i], kf);
+    float d = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) d = fmaf(qf[e], kf[e], d);
+    sc[i] = d;
+  }
+  transpose_reduce<NR, LPR>(sc, lane);
+  // lane holds the score of tile row g + RPL * idx, idx = (lane % LPR) / (LPR / NR)
+  const int idx = c / (LPR / NR);
+  const int my_row = base + g + RPL * idx;
+  const float sv = my_row < k1 ? sc[0] : -INFINITY;
+  const float m_new = fmaxf(m_run, warp_max(sv));
+  const float alpha = ex2(m_run - m_new);
+  const float pr = ex2(sv - m_new);
+  const float psum = warp_sum((c % (LPR / NR)) == 0 ? pr : 0.f);
+  l_run = l_run * alpha + psum;
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) acc[e] *= alpha;
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const float pi = __shfl_sync(0xffffffffu, pr, g * LPR + i * (LPR / NR));
+    float vf[EPV];
+    Vec16<T>::to_float(vv[i], vf);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[e] = fmaf(pi, vf[e], acc[e]);
+  }
+  m_run = m_new;
+}
+
+template <typename T, int A>
+__device__ __forceinline__ void load_q(const AttnArgs& a, int t, int h, int c, float (&qf)[Vec16<T>::N]) {
+  constexpr int EPV = Vec16<T>::N;
+  const uint4 qv = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + (size_t(t) * a.num_heads + h) * A +
+                                                   c * EPV);
+  Vec16<T>::to_float(qv, qf);
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) qf[e] *= a.scale_log2;    // scores in the exp2 domain
+}
+
+// Loads straight to registers: any dtype, head_dim 64/128, any block size.
+template <typename T, int A, bool ROW_MODE>
+__global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs sa) {
+  constexpr int EPV = Vec16<T>::N;        // elements per 16-byte load
+  constexpr int LPR = A / EPV;            // lanes per key row
+  constexpr int RPL = 32 / LPR;           // key rows per warp load
+  constexpr int NR = kTile / RPL;         // key rows per lane per tile
+  static_assert(NR <= LPR && NR >= 1, "tile shape");
+  const AttnArgs& a = sa.a;
+  const int split = blockIdx.x, h = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  RowPlan pl;
+  if (!plan_row<ROW_MODE>(a, split, h, pl)) return;
+  const int g = lane / LPR, c = lane % LPR;
+  float qf[EPV];
+  load_q<T, A>(a, pl.t, h, c, qf);
 
   const T* kp = static_cast<const T*>(a.k_pool);
   const T* vp = static_cast<const T*>(a.v_pool);
-  const int32_t* bt = a.block_tables + size_t(s) * a.max_blocks_per_seq;
+  const int32_t* bt = a.block_tables + size_t(pl.s) * a.max_blocks_per_seq;
   const int B = a.block_size;
   const size_t head_off = size_t(h) * B * A;
   const size_t blk_stride = size_t(a.num_heads) * B * A;
   const bool whole_tiles = (B % kTile) == 0;
-
   float m_run = -INFINITY, l_run = 0.f;
   float acc[EPV];
 #pragma unroll
   for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
 
-  for (int base = k0 + warp * kTile; base < k1; base += kWarps * kTile) {
+  for (int base = pl.k0 + warp * kTile; base < pl.k1; base += kWarps * kTile) {
     uint4 kv[NR], vv[NR];
     int32_t tile_blk = 0;
     if (whole_tiles) {
@@ -163,7 +303,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs s
       const int j = base + g + RPL * i;
       kv[i] = make_uint4(0, 0, 0, 0);
       vv[i] = make_uint4(0, 0, 0, 0);
-      if (j < k1) {
+      if (j < pl.k1) {
         int32_t blk = tile_blk;
         if (!whole_tiles) {
           blk = bt[j / B];
@@ -179,112 +319,101 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs s
         }
       }
     }
-    float sc[NR];
-#pragma unroll
-    for (int i = 0; i < NR; ++i) {
-      float kf[EPV];
-      Vec16<T>::to_float(kv[i], kf);
-      float d = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) d = fmaf(qf[e], kf[e], d);
-      sc[i] = d;
-    }
-    transpose_reduce<NR, LPR>(sc, lane);
-    // lane holds the score of tile row g + RPL * idx, idx = (lane % LPR) / (LPR / NR)
-    const int idx = c / (LPR / NR);
-    const int my_row = base + g + RPL * idx;
-    const float sv = my_row < k1 ? sc[0] : -INFINITY;
-    const float m_new = fmaxf(m_run, warp_max(sv));
-    const float alpha = ex2(m_run - m_new);
-    const float pr = ex2(sv - m_new);
-    const float psum = warp_sum((c % (LPR / NR)) == 0 ? pr : 0.f);
-    l_run = l_run * alpha + psum;
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) acc[e] *= alpha;
-#pragma unroll
-    for (int i = 0; i < NR; ++i) {
-      const float pi = __shfl_sync(0xffffffffu, pr, g * LPR + i * (LPR / NR));
-      float vf[EPV];
-      Vec16<T>::to_float(vv[i], vf);
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) acc[e] = fmaf(pi, vf[e], acc[e]);
-    }
-    m_run = m_new;
+    tile_update<T, EPV, LPR, RPL, NR>(qf, kv, vv, base, pl.k1, lane, m_run, l_run, acc);
   }
-  // lanes of different row groups hold the same chunk: add them
-#pragma unroll
-  for (int o = LPR; o < 32; o <<= 1) {
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
-  }
-
-  __shared__ float sm_acc[kWarps][A];
-  __shared__ float sm_m[kWarps], sm_l[kWarps];
-  __shared__ int sm_last;
-  if (g == 0) {
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) sm_acc[warp][c * EPV + e] = acc[e];
-  }
-  if (lane == 0) {
-    sm_m[warp] = m_run;
-    sm_l[warp] = l_run;
-  }
-  __syncthreads();
-
-  const int d = threadIdx.x;
-  float M = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w]);
-  float L = 0.f, o = 0.f;
-  if (d < A) {
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float f = ex2(sm_m[w] - M);   // a warp with no keys has m = -inf: weight 0
-      L = fmaf(sm_l[w], f, L);
-      o = fmaf(sm_acc[w][d], f, o);
-    }
-  }
-  T* out_row = static_cast<T*>(a.out) + (size_t(t) * a.num_heads + h) * A;
-  if (nsplit == 1) {
-    if (d < A) {
-      const float r = o / L;
-      store1(out_row + d, r);
-    }
-    return;
-  }
-  const int row_id = ROW_MODE ? t : s;
-  float* part = sa.partials + ((size_t(row_id) * a.num_heads + h) * sa.max_splits) * (A + 2);
-  if (d < A) part[size_t(split) * (A + 2) + d] = o;
-  if (d == 0) {
-    part[size_t(split) * (A + 2) + A] = M;
-    part[size_t(split) * (A + 2) + A + 1] = L;
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int32_t* ticket = sa.tickets + size_t(row_id) * a.num_heads + h;
-    sm_last = atomicAdd(ticket, 1) == nsplit - 1;
-    if (sm_last) *ticket = 0;             // every split has arrived: reset for the next call
-  }
-  __syncthreads();
-  if (!sm_last) return;
-  __threadfence();
-  if (d < A) {
-    float MM = -INFINITY;
-    for (int k = 0; k < nsplit; ++k) MM = fmaxf(MM, __ldcg(part + size_t(k) * (A + 2) + A));
-    float LL = 0.f, oo = 0.f;
-    for (int k = 0; k < nsplit; ++k) {
-      const float* pk = part + size_t(k) * (A + 2);
-      const float f = ex2(__ldcg(pk + A) - MM);
-      LL = fmaf(__ldcg(pk + A + 1), f, LL);
-      oo = fmaf(__ldcg(pk + d), f, oo);
-    }
-    const float r = oo / LL;
-    store1(out_row + d, r);
-  }
+  __shared__ MergeSmem<A> sm;
+  finish_split<T, A, ROW_MODE, EPV, LPR>(sa, pl, split, h, m_run, l_run, acc, sm);
 }
 
+// Decode rows, bf16, head_dim 128, block size a multiple of 16: each warp
+// streams its 16-key K/V tiles (4 KB each, contiguous in the pool) with bulk
+// async copies into a private kStages-deep shared ring, kStages tiles ahead.
+__global__ void __launch_bounds__(kWarps * 32) split_kv_bulk_kernel(const SplitArgs sa) {
+  using T = __nv_bfloat16;
+  constexpr int A = 128, EPV = 8, LPR = 16, RPL = 2, NR = 8;
+  const AttnArgs& a = sa.a;
+  const int split = blockIdx.x, h = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  RowPlan pl;
+  if (!plan_row<false>(a, split, h, pl)) return;
+  const int g = lane / LPR, c = lane % LPR;
+  float qf[EPV];
+  load_q<T, A>(a, pl.t, h, c, qf);
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem + warp * kStages * 2 * kTileBytes;                  // [stage][K | V]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * 2 * kTileBytes) + warp * kStages;
+  int* valid = reinterpret_cast<int*>(smem + kWarps * kStages * 2 * kTileBytes + kWarps * kStages * 8) +
+               warp * kStages;
+  MergeSmem<A>& sm = *reinterpret_cast<MergeSmem<A>*>(smem + kWarps * kStages * 2 * kTileBytes +
+                                                      kWarps * kStages * 8 + kWarps * kStages * 4);
+  const T* kp = static_cast<const T*>(a.k_pool);
+  const T* vp = static_cast<const T*>(a.v_pool);
+  const int32_t* bt = a.block_tables + size_t(pl.s) * a.max_blocks_per_seq;
+  const int B = a.block_size;
+  const size_t head_off = size_t(h) * B * A;
+  const size_t blk_stride = size_t(a.num_heads) * B * A;
+  const int ntiles = (pl.k1 - pl.k0 + kTile - 1) / kTile;   // tiles of the split; warp takes w, w+4, ...
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) sm100::mbar_init(sm100::smem_u32(&bars[st]), 1);
+    sm100::fence_mbar_init();
+  }
+  __syncwarp();
+  // lane 0: copy the warp's it-th tile into ring slot it % kStages
+  auto issue = [&](int it) {
+    const int j0 = pl.k0 + (warp + kWarps * it) * kTile;
+    const int st = it % kStages;
+    const uint32_t bar = sm100::smem_u32(&bars[st]);
+    const int blk = bt[j0 / B];
+    if (blk >= 0 && blk < a.num_blocks) {
+      valid[st] = 1;
+      const size_t off = size_t(blk) * blk_stride + head_off + size_t(j0 % B) * A;
+      const uint32_t dst = sm100::smem_u32(ring + st * 2 * kTileBytes);
+      sm100::mbar_arrive_expect_tx(bar, 2 * kTileBytes);
+      sm100::bulk_load(dst, kp + off, kTileBytes, bar);
+      sm100::bulk_load(dst + kTileBytes, vp + off, kTileBytes, bar);
+    } else {
+      raise_error(a.err, kErrBounds);
+      valid[st] = 0;
+      sm100::mbar_arrive(bar);
+    }
+  };
+  if (lane == 0)
+    for (int it = 0; it < kStages && warp + kWarps * it < ntiles; ++it) issue(it);
+
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[EPV];
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
+  for (int it = 0; warp + kWarps * it < ntiles; ++it) {
+    const int st = it % kStages;
+    if (!__all_sync(0xffffffffu, sm100::mbar_wait(sm100::smem_u32(&bars[st]), (it / kStages) & 1))) {
+      if (lane == 0) raise_error(a.err, kErrTimeout);
+      break;
+    }
+    const int base = pl.k0 + (warp + kWarps * it) * kTile;
+    const bool ok = valid[st] != 0;
+    const uint8_t* kt = ring + st * 2 * kTileBytes;
+    uint4 kv[NR], vv[NR];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      const int r = g + RPL * i;
+      const bool in = ok && base + r < pl.k1;
+      kv[i] = in ? *reinterpret_cast<const uint4*>(kt + r * 256 + c * 16) : make_uint4(0, 0, 0, 0);
+      vv[i] = in ? *reinterpret_cast<const uint4*>(kt + kTileBytes + r * 256 + c * 16) : make_uint4(0, 0, 0, 0);
+    }
+    tile_update<T, EPV, LPR, RPL, NR>(qf, kv, vv, base, pl.k1, lane, m_run, l_run, acc);
+    __syncwarp();                         // every lane has used what it read: the slot may be refilled
+    if (lane == 0 && warp + kWarps * (it + kStages) < ntiles) issue(it + kStages);
+  }
+  finish_split<T, A, false, EPV, LPR>(sa, pl, split, h, m_run, l_run, acc, sm);
+}
+
+constexpr uint32_t kBulkSmem = kWarps * kStages * 2 * kTileBytes + kWarps * kStages * (8 + 4) +
+                               sizeof(MergeSmem<128>);
+
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+bool g_bulk_attr[64] = {};
 
 }  // namespace
 
@@ -325,7 +454,17 @@ cb_status launch_split_kv(const AttnArgs& a, bool row_mode, void* workspace,
   }
   dim3 grid(unsigned(sa.max_splits), unsigned(a.num_heads), unsigned(rows));
   const bool bf16 = a.dtype == CB_DTYPE_BF16;
-  if (bf16 && a.head_dim == 128) {
+  if (!row_mode && bf16 && a.head_dim == 128 && a.block_size % kTile == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !g_bulk_attr[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(split_kv_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(kBulkSmem));
+      if (e != cudaSuccess) return cuda_fail(e, "split-KV: shared memory attribute");
+      g_bulk_attr[dev] = true;
+    }
+    split_kv_bulk_kernel<<<grid, kWarps * 32, kBulkSmem, stream>>>(sa);
+  } else if (bf16 && a.head_dim == 128) {
     row_mode ? launch<__nv_bfloat16, 128, true>(sa, grid, stream)
              : launch<__nv_bfloat16, 128, false>(sa, grid, stream);
   } else if (bf16 && a.head_dim == 64) {
