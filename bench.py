@@ -542,10 +542,15 @@ def main():
     api.cb_check_device_errors()
 
     # roofline of the dominant kernel and of the whole step
-    if b.max_q_len == 1 or args.workload == "decode":
-        dom = {"kernel": "split_kv_kernel (decode rows)", "bound": "hbm",
-               "achieved": work["decode_bytes"] / (attn_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
-               "unit": "GB/s"}
+    # dominant kernel: the larger of the decode rows' HBM time and the prefill
+    # chunks' tensor time (both kernels run inside the one attention call, so
+    # in a mixed step the call time bounds the dominant kernel's time from above)
+    t_dec = work["decode_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_pre = work["prefill_flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_dec >= t_pre:
+        dom = {"kernel": "split_kv_bulk_kernel (decode rows)" if b.dtype == "bf16" else "split_kv_kernel",
+               "bound": "hbm", "achieved": work["decode_bytes"] / (attn_ms * 1e-3) / 1e9,
+               "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
         dom = {"kernel": "prefill_tc_kernel (prefill chunks)", "bound": "tensor",
                "achieved": work["prefill_flops"] / (attn_ms * 1e-3) / 1e12,

@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcb.so")
 
 CUDA_SOURCES = ["runtime.cu", "append_kv.cu", "split_kv.cu", "prefill_tc.cu", "attention.cu",
-                "synth.cu", "decode_noalloc.cu"]
+                "synth.cu", "decode_noalloc.cu", "selftest.cu"]
 CXX_SOURCES = ["scheduler.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O3",

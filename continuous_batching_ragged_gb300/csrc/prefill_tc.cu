@@ -377,27 +377,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN; ++c)
           if (kb + c > limit) sr[c] = __float_as_uint(-INFINITY);
       }
+      {                                            // four independent max chains (latency, not issue, bound)
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < BN; c += 2) mt = max3(mt, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+        for (int c = 0; c < BN; c += 8)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            m4[u] = max3(m4[u], __uint_as_float(sr[c + 2 * u]), __uint_as_float(sr[c + 2 * u + 1]));
+        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      }
       const float m_new = fmaxf(m, mt * sl2);
       const bool resc = m_new > m + 8.0f;         // keep a stale max while exp2 stays <= 2^8
       const float m_use = resc ? m_new : m;
       const float alpha = resc ? ex2(m - m_new) : 1.0f;
       const uint64_t scale2 = f2_pack(sl2, sl2);
       const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
-      uint64_t sum2 = f2_pack(0.f, 0.f);
+      uint64_t sum2[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < 64; ++c) {               // P packed in place over the scores
         float x0, x1;
         f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), scale2, neg_m2),
                   x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
-        sum2 = f2_add(sum2, f2_pack(p0, p1));
+        sum2[c & 3] = f2_add(sum2[c & 3], f2_pack(p0, p1));
         sr[c] = pack_bf16x2(p0, p1);
       }
-      float rs0, rs1;
-      f2_unpack(sum2, rs0, rs1);
-      const float rs = rs0 + rs1;
+      float rs0, rs1, rs2, rs3, rs4, rs5, rs6, rs7;
+      f2_unpack(sum2[0], rs0, rs1);
+      f2_unpack(sum2[1], rs2, rs3);
+      f2_unpack(sum2[2], rs4, rs5);
+      f2_unpack(sum2[3], rs6, rs7);
+      const float rs = ((rs0 + rs1) + (rs2 + rs3)) + ((rs4 + rs5) + (rs6 + rs7));
       l = l * alpha + rs;
       m = m_use;
       tc_fence_before();

@@ -22,7 +22,7 @@ EXPORTS = ("cb_append_kv", "cb_attention_workspace_size", "cb_ragged_attention",
            "cb_decode_attention_noalloc",
            "cb_scheduler_create", "cb_scheduler_destroy", "cb_add_request", "cb_build_batch",
            "cb_complete_step", "cb_scheduler_stats", "cb_check_device_errors", "cb_last_error",
-           "cb_synth_tokens", "cb_synth_fill_cache")
+           "cb_synth_tokens", "cb_synth_fill_cache", "cb_selftest_bounded_wait")
 
 
 class cb_kv_cache(ctypes.Structure):
@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
         "cb_scheduler_stats": (st, [vp, ctypes.POINTER(cb_sched_stats)]),
         "cb_check_device_errors": (st, [vp]),
         "cb_last_error": (ctypes.c_char_p, []),
+        "cb_selftest_bounded_wait": (st, [i32, vp]),
         "cb_synth_tokens": (st, [vp, ctypes.c_int, u64, i32, i32, vp, vp, i32, i32, i32, vp]),
         "cb_synth_fill_cache": (st, [vp, ctypes.c_int, u64, i32, i32, vp, vp, vp, i32, i32, i32, i32,
                                      i32, i32, i32, vp]),

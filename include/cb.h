@@ -236,6 +236,16 @@ cb_status cb_scheduler_stats(const cb_scheduler* sched, cb_sched_stats* out);
 cb_status cb_check_device_errors(void* stream);
 const char* cb_last_error(void);
 
+/* ---------------------------------------------------------------------------
+ * cb_selftest_bounded_wait -- failure-detection self test.
+ * Not a step of the method: launches one CTA that waits, with the same
+ * bounded mbarrier wait the kernels use for every pipeline hand-off, on a
+ * barrier nothing ever arrives at.  After timeout_ms (1..10000) the wait gives
+ * up, the CTA sets CB_ERR_TIMEOUT on the device error word and exits, so the
+ * context stays usable; cb_check_device_errors then returns CB_ERR_TIMEOUT.
+ * ------------------------------------------------------------------------- */
+cb_status cb_selftest_bounded_wait(int32_t timeout_ms, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
