@@ -64,10 +64,27 @@ def algorithmic_work(b):
     decode = b.q_len == 1
     dec_bytes = (int(np.sum(b.context_lens[decode].astype(np.int64))) * 2 * H * A * e
                  + int(np.sum(decode)) * H * A * e * 2)
+    pre = b.q_len > 1
+    pre_bytes = (int(np.sum(b.context_lens[pre].astype(np.int64))) * 2 * H * A * e
+                 + int(np.sum(b.q_len[pre])) * H * A * e * 2)
     return {"bytes": kv_read + qo + append, "flops": flops, "decode_bytes": dec_bytes,
+            "prefill_bytes": pre_bytes,
             "append_bytes": append,
             "prefill_flops": 4 * A * H * sum(int(q) * int(p) + int(q) * (int(q) + 1) // 2
                                              for p, q in zip(b.p, b.q_len) if q > 1)}
+
+
+def profiled_traffic_ratio(profile: str):
+    """DRAM bytes per algorithmic byte recorded from an ncu capture of the
+    kernel (dram__bytes_read.sum + dram__bytes_write.sum over the same
+    algorithmic bytes model), or None if no summary records it."""
+    path = os.path.join(ROOT, "profiles", profile)
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        if line.startswith("dram_bytes_per_algorithmic_byte:"):
+            return float(line.split(":", 1)[1])
+    return None
 
 
 def load_peaks():
@@ -556,7 +573,15 @@ def main():
                "achieved": work["prefill_flops"] / (attn_ms * 1e-3) / 1e12,
                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     dom["frac"] = dom["achieved"] / dom["peak"]
-    dom["traffic"] = None
+    if dom["bound"] == "hbm":
+        prof, alg = "split_kv_bulk_decode_64seq.md", work["decode_bytes"]
+    else:
+        prof, alg = "prefill_tc_long_prompt_last_chunk.md", work["prefill_bytes"]
+    ratio = profiled_traffic_ratio(prof) if b.dtype == "bf16" else None
+    dom["traffic"] = None if ratio is None else ratio * alg
+    if ratio is not None:
+        dom["traffic_source"] = (f"profiles/{prof}: dram bytes per algorithmic byte of an ncu capture "
+                                 f"({ratio}), times this launch's {alg} algorithmic bytes")
     dom["peak_source"] = f"of {peaks['source']}"
     t_hbm = work["bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_tc = work["flops"] / (peaks["bf16_tflops"] * 1e12)
