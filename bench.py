@@ -346,6 +346,26 @@ def trace_step_roofline(step, num_layers, num_heads, head_dim, peaks):
 # main
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(x: float) -> float:
+    """The slowest rank's value (identity without a process group).  Uses the
+    group's own device: CUDA tensors under NCCL, CPU tensors under gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_rank: int, slowest_ms: float, world: int) -> float:
+    """Whole-job tokens/s of N independent replicas (weak scaling): every rank
+    serves the same step, so the job completes world * tokens in the slowest
+    rank's time."""
+    return world * tokens_per_rank / (slowest_ms * 1e-3)
+
+
 def dist_info():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -523,11 +543,8 @@ def main():
     attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * b.T / (ms * 1e-3)
+    ms = max_over_ranks(ms)
+    value = replica_throughput(b.T, ms, world)
 
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs and metadata, the two calls, D2H of the output
@@ -555,7 +572,7 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
     api.cb_check_device_errors()
 
     # roofline of the dominant kernel and of the whole step
@@ -607,7 +624,7 @@ def main():
                            if work["bytes"] > 1e9 else "inputs smaller than L2; no flush",
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "roofline": dom, "step_roofline": step_roof, "cpu_baseline": cpu,
-                "e2e": {"value": world * b.T / (e2e_ms * 1e-3), "unit": UNIT,
+                "e2e": {"value": replica_throughput(b.T, e2e_ms, world), "unit": UNIT,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "clocks": clocks, "gpu_launches": launches_per_step * args.steps}
         print(json.dumps(line), flush=True)
