@@ -49,6 +49,13 @@ def make_workload(name: str, decode_seqs: int = 256):
         return W.long_prompt_chunk(15), "long_prompt_32768_last_chunk_2048_bf16_H32_A128_B16"
     if name == "tiny":
         return W.tiny_fp32(), "tiny_fp32_H4_A64_B4_T6"
+    if name == "mixed_padded":
+        return W.padded_equivalent(W.mixed_step()), "mixed_m2048_left_padded_to_67x662_bf16_H32_A128_B16"
+    if name == "insertion":
+        return W.page_insertion_example(), "insertion_B8_n100_ragged_bf16_H32_A128_B16"
+    if name == "insertion_padded":
+        return (W.padded_equivalent(W.page_insertion_example()),
+                "insertion_B8_n100_left_padded_8x100_bf16_H32_A128_B16")
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -473,7 +480,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "mixed", "long", "tiny", "trace"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "mixed", "long", "tiny", "trace", "mixed_padded", "insertion", "insertion_padded"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-seqs", type=int, default=256,
@@ -544,7 +551,8 @@ def main():
     append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     ms = total_ms / args.steps
     ms = max_over_ranks(ms)
-    value = replica_throughput(b.T, ms, world)
+    useful = b.useful_tokens if b.useful_tokens is not None else b.T
+    value = replica_throughput(useful, ms, world)
 
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs and metadata, the two calls, D2H of the output
@@ -618,13 +626,14 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": b.dtype, "data": "synthetic",
-                "config": {"workload": label, "num_seqs": b.num_seqs, "tokens_per_step": b.T,
+                "config": {"workload": label, "num_seqs": b.num_seqs, "tokens_per_step": useful,
+                           "computed_query_rows": b.T,
                            "kv_bytes_read": int(work["bytes"] - work["append_bytes"]),
                            "l2": "inputs larger than L2 (KV cache read per step >> 129 MB)"
                            if work["bytes"] > 1e9 else "inputs smaller than L2; no flush",
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "roofline": dom, "step_roofline": step_roof, "cpu_baseline": cpu,
-                "e2e": {"value": replica_throughput(b.T, e2e_ms, world), "unit": UNIT,
+                "e2e": {"value": replica_throughput(useful, e2e_ms, world), "unit": UNIT,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "clocks": clocks, "gpu_launches": launches_per_step * args.steps}
         print(json.dumps(line), flush=True)

@@ -142,6 +142,7 @@ class RaggedBatch:
     block_tables: np.ndarray        # [S, max_blocks] int32, -1 padded
     num_blocks: int                 # pool size in blocks
     name: str = ""
+    useful_tokens: Optional[int] = None   # of a padded batch: the real query tokens
 
     @property
     def num_seqs(self) -> int:
@@ -258,6 +259,36 @@ def make_batch(p: Sequence[int], q_len: Sequence[int], *, num_heads: int, head_d
                        dtype=dtype, seed=seed, layer=layer,
                        seq_ids=np.asarray(seq_ids, dtype=np.int64), p=p, q_len=q_len,
                        block_tables=bt, num_blocks=nb, name=name)
+
+
+def padded_equivalent(b: RaggedBatch) -> RaggedBatch:
+    """The same sequences as one rectangular, left-padded batch: every sequence
+    carries max(q_len) new tokens, its real ones last, so a step computes
+    B * max(q_len) query rows and the pad tokens' keys.  (Hugging Face blog
+    "Continuous batching from first principles", section "Continuous
+    batching": inserting an n-token prompt into B decoding prompts costs
+    (n-1)(B-1) padding tokens.)"""
+    n = int(b.q_len.max())
+    pb = make_batch(b.p, np.full(b.num_seqs, n, np.int64), num_heads=b.num_heads, head_dim=b.head_dim,
+                    block_size=b.block_size, dtype=b.dtype, seed=b.seed, layer=b.layer,
+                    seq_ids=b.seq_ids, name=b.name + "_padded")
+    pb.useful_tokens = b.T
+    return pb
+
+
+def padding_tokens(b: RaggedBatch) -> int:
+    """Query rows the padded equivalent adds over the ragged batch."""
+    return int(b.num_seqs * b.q_len.max() - b.q_len.sum())
+
+
+def page_insertion_example(seed: int = 5, batch: int = 8, n: int = 100, cached: int = 512,
+                           num_heads: int = 32, head_dim: int = 128, block_size: int = 16) -> RaggedBatch:
+    """B-1 prompts decoding one token each (``cached`` tokens in the cache) plus
+    one newly inserted prompt of n tokens, the blog's B=8, n=100 example."""
+    p = [cached] * (batch - 1) + [0]
+    q = [1] * (batch - 1) + [n]
+    return make_batch(p, q, num_heads=num_heads, head_dim=head_dim, block_size=block_size,
+                      dtype="bf16", seed=seed, name="insertion")
 
 
 # ---------------------------------------------------------------------------

@@ -56,3 +56,16 @@ def test_batch_metadata_shapes():
     assert m.q_len[-3:].tolist() == [661, 661, 662] and m.p[-3:].tolist() == [0, 1024, 2048]
     d = w.decode_step(num_seqs=16)
     assert np.all((d.p >= 512) & (d.p <= 4096))
+
+
+def test_padding_count_matches_the_blog_example():
+    """Blog 'Continuous batching from first principles', section 'Continuous
+    batching': B=8, n=100 -> (n-1)(B-1) = 693 padding tokens."""
+    b = w.page_insertion_example()
+    assert b.T == 7 + 100
+    assert w.padding_tokens(b) == 693 == (100 - 1) * (8 - 1)
+    pb = w.padded_equivalent(b)
+    assert pb.T == 8 * 100 and pb.T - b.T == 693
+    # the real tokens keep their positions: each sequence's last rows are its real ones
+    assert np.array_equal(pb.context_lens - pb.q_len, b.p)
+    assert np.array_equal(pb.context_lens[:-1], b.p[:-1] + 100)
