@@ -329,11 +329,20 @@ def run_trace(torch, api, W, requests, *, num_layers, num_heads, head_dim, block
     return steps
 
 
+def attention_launches(num_seqs, num_tokens, max_q_len, dtype="bf16"):
+    """Kernels cb_ragged_attention launches for one call, by its routing: fp32
+    runs one row-mode kernel; bf16 runs the step plan, then the decode kernel
+    (max_q_len == 1), the prefill kernel (one sequence, all prefill) or both."""
+    if dtype != "bf16":
+        return 1
+    if max_q_len == 1 or (num_seqs == 1 and max_q_len == num_tokens):
+        return 2
+    return 3
+
+
 def launches_per_layer(st):
     """Kernels cb_append_kv + cb_ragged_attention launch for one layer of a step."""
-    prefill = st["max_q_len"] > 1
-    decode = not prefill or not (st["S"] == 1 and st["max_q_len"] == st["T"])
-    return 1 + int(prefill) + int(decode)
+    return 1 + attention_launches(st["S"], st["T"], st["max_q_len"])
 
 
 def trace_step_roofline(step, num_layers, num_heads, head_dim, peaks):
@@ -522,7 +531,7 @@ def main():
     api.cb_check_device_errors()
     torch.cuda.synchronize()
 
-    launches_per_step = 2 + (1 if b.max_q_len > 1 and np.any(b.q_len == 1) else 0)
+    launches_per_step = 1 + attention_launches(b.num_seqs, b.T, b.max_q_len, b.dtype)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     sampler = ClockSampler(dev_index)

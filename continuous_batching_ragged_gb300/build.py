@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcb.so")
 
-CUDA_SOURCES = ["runtime.cu", "append_kv.cu", "split_kv.cu", "prefill_tc.cu", "attention.cu",
+CUDA_SOURCES = ["runtime.cu", "append_kv.cu", "plan.cu", "split_kv.cu", "prefill_tc.cu", "attention.cu",
                 "synth.cu", "decode_noalloc.cu", "selftest.cu"]
 CXX_SOURCES = ["scheduler.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -6,9 +6,12 @@
 // kernel splits the work by request.  Here a request's rows go to one of two
 // kernels by shape: q_len == 1 (decode) to split-KV on CUDA cores, which is
 // bound by HBM; q_len > 1 (a prefill chunk) to tcgen05 tensor cores, which is
-// a dense contraction.  The two run concurrently on two streams joined by
-// events, so a mixed step costs about the longer of the two, not the sum.
-// fp32 caches take the CUDA-core kernel for every row.
+// a dense contraction.  A one-CTA plan kernel first lists the step's work
+// units on the GPU; both attention kernels are persistent grids that claim
+// those units, so the launch shape does not depend on the batch.  In a mixed
+// step the two run on two streams joined by events, and whichever finishes
+// its list first leaves its SMs to the other.  fp32 caches take the CUDA-core
+// kernel for every row.
 #include <cmath>
 
 #include "kernels.h"
@@ -101,8 +104,16 @@ extern "C" cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache
 
   if (cache->dtype == CB_DTYPE_F32) return cb::launch_split_kv(a, true, workspace, workspace_bytes, main);
 
-  if (max_q_len == 1) return cb::launch_split_kv(a, false, workspace, workspace_bytes, main);
-  if (max_q_len == num_tokens && num_seqs == 1) return cb::launch_prefill_tc(a, main);
+  // bf16: the step plan first, then the persistent kernels over its work lists
+  cb::StepPlan plan;
+  st = cb::step_plan_layout(workspace, workspace_bytes, num_seqs, num_tokens, cache->num_heads,
+                            cache->head_dim, max_context_len, &plan);
+  if (st != CB_OK) return st;
+  plan.dec_ctas = cb::decode_persistent_ctas();
+  st = cb::launch_plan(a, plan, main);
+  if (st != CB_OK) return st;
+  if (max_q_len == 1) return cb::launch_decode_persistent(a, plan, true, main);
+  if (max_q_len == num_tokens && num_seqs == 1) return cb::launch_prefill_tc(a, plan, true, main);
 
   // Mixed step: prefill chunks on the auxiliary stream, decode rows on `stream`.
   cb::AuxStream* aux = cb::aux_stream();
@@ -114,8 +125,8 @@ extern "C" cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache
     cb::unlock_aux();
     return cb::cuda_fail(e, "forking the auxiliary stream");
   }
-  cb_status sp = cb::launch_prefill_tc(a, aux->stream);
-  cb_status sd = cb::launch_split_kv(a, false, workspace, workspace_bytes, main);
+  cb_status sp = cb::launch_prefill_tc(a, plan, false, aux->stream);
+  cb_status sd = cb::launch_decode_persistent(a, plan, false, main);
   e = cudaEventRecord(aux->join, aux->stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(main, aux->join, 0);
   cb::unlock_aux();

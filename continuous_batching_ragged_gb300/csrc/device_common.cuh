@@ -14,6 +14,25 @@ constexpr unsigned kErrBounds = 1u;
 constexpr unsigned kErrTimeout = 2u;
 constexpr unsigned kErrInvalid = 4u;
 
+// With kErrTimeout, bits 8 and up name the wait that ran out (one bit per
+// site, OR-ed over every CTA that gave up), for the error message.
+enum : unsigned {
+  kSiteDecodeRing = 1u << 8,
+  kSitePfItemFree = 1u << 9,     // prefill K loader: item slot release
+  kSitePfKFree = 1u << 10,       // prefill K loader: K stage release
+  kSitePfQFree = 1u << 11,       // prefill K loader: Q release
+  kSitePfItem = 1u << 12,        // prefill V loader / MMA / softmax: item publication
+  kSitePfVFree = 1u << 13,       // prefill V loader: V stage release
+  kSitePfVTail = 1u << 14,       // prefill V loader: tail tile landing
+  kSitePfQ = 1u << 15,           // prefill MMA: Q landing
+  kSitePfK = 1u << 16,           // prefill MMA: K landing
+  kSitePfV = 1u << 17,           // prefill MMA: V landing
+  kSitePfP = 1u << 18,           // prefill MMA: P written
+  kSitePfS = 1u << 19,           // prefill softmax: S ready
+  kSitePfO = 1u << 20,           // prefill softmax: P V done
+  kSiteSelfTest = 1u << 21,
+};
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void raise_error(unsigned* word, unsigned bits) {

@@ -31,9 +31,54 @@ struct AttnArgs {
   unsigned* err;
 };
 
-// Keys per split of the split-KV kernel.  The split plan of a row depends only
-// on that row's own number of visible keys.
+// Keys per split of the register split-KV kernel, and the smallest split of
+// the persistent decode kernel (whose split length the step plan chooses per
+// step and stores in header[5]).  Workspaces are sized for this split.
 constexpr int kSplitKeys = 512;
+
+// Query rows per work item of the prefill kernel (two 128-row tiles).
+constexpr int kPrefillPairRows = 256;
+
+// The step's work lists, built on the GPU from the packed metadata by
+// launch_plan and consumed by the persistent decode and prefill kernels, which
+// claim items through the counters in `header`.  All pointers are into the
+// caller's workspace.
+struct StepPlan {
+  int32_t* header;        // [0] decode items, [1] prefill items, [2] decode claims, [3] prefill claims,
+                          // [4] call tag, [5] keys per decode split
+  int2* dec_items;        // (sequence, split) of every q_len == 1 row, longest first
+  int2* dec_scratch;      // the decode items before sorting
+  int2* pre_items;        // (sequence, 256-row query pair) of every q_len > 1 chunk, costliest first
+  int2* pre_scratch;      // the prefill items before sorting
+  int32_t* tickets;       // [num_seqs][H] split arrival counters, zeroed by the plan
+  float* partials;        // [num_seqs][H][max_splits][A + 2] split results (acc, max, sum)
+  int32_t max_splits;
+  int32_t dec_cap;        // capacity of dec_items
+  int32_t pre_cap;        // capacity of pre_items and pre_scratch
+  uint32_t tag;           // this call's tag: the plan writes it to header[4], the kernels check it
+  int32_t dec_ctas;       // CTAs of the persistent decode grid (sets the split length)
+};
+
+// Workspace of a bf16 step (plan + split scratch) and its carving.
+size_t step_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_heads, int32_t head_dim,
+                            int32_t max_context_len);
+cb_status step_plan_layout(void* workspace, size_t workspace_bytes, int32_t num_seqs, int32_t num_tokens,
+                           int32_t num_heads, int32_t head_dim, int32_t max_context_len, StepPlan* plan);
+
+// One CTA: validates every sequence's metadata (flagging bad rows in the
+// error word and leaving them out), fills the work lists and clears the
+// claim counters and the split tickets.  Dependent kernels launched with
+// launch_after_plan may start while it runs and wait for it on the device.
+cb_status launch_plan(const AttnArgs& a, const StepPlan& plan, cudaStream_t stream);
+
+// CTAs of the persistent decode grid on the current device (0 on error).
+int decode_persistent_ctas();
+
+// Persistent decode over the plan's decode items (bf16, head_dim 128, block
+// size a multiple of 16).  `after_plan`: launched right behind launch_plan on
+// the same stream, overlapping its launch with the plan.
+cb_status launch_decode_persistent(const AttnArgs& a, const StepPlan& plan, bool after_plan,
+                                   cudaStream_t stream);
 
 // Split-KV attention on CUDA cores.  Decode mode: one query row per sequence
 // with q_len == 1 (other sequences are left to the prefill kernel).  Row mode:
@@ -43,7 +88,8 @@ size_t split_kv_workspace_bytes(bool row_mode, int32_t num_seqs, int32_t num_tok
 cb_status launch_split_kv(const AttnArgs& a, bool row_mode, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream);
 
-// Prefill chunks (q_len > 1) on tcgen05 tensor cores, bf16, head_dim 128.
-cb_status launch_prefill_tc(const AttnArgs& a, cudaStream_t stream);
+// Prefill chunks (q_len > 1) on tcgen05 tensor cores, bf16, head_dim 128:
+// persistent CTAs over the plan's prefill items.
+cb_status launch_prefill_tc(const AttnArgs& a, const StepPlan& plan, bool after_plan, cudaStream_t stream);
 
 }  // namespace cb

@@ -1,0 +1,270 @@
+// The step plan: work lists for the persistent attention kernels, built on
+// the GPU from the packed metadata.
+//
+// Page "continuous-batching" (zhangchitc.github.io), section "Inside the
+// kernel": the loops over requests and over each request's cache become the
+// kernel's parallel units.  Here the units are listed explicitly, once per
+// step, so the attention kernels can run a fixed grid (one or two CTAs per SM)
+// that claims units until the lists run out: no CTA is launched for a unit
+// that does not exist (a split past a short context, a prefill tile of a
+// decode row), and the launch shape no longer depends on the batch, which is
+// what lets a whole step be captured once in a CUDA graph.
+//   * decode items: (sequence, split) for every q_len == 1 row, one per 512
+//     keys of its context, in sequence order;
+//   * prefill items: (sequence, pair of 128-row query tiles) for every
+//     q_len > 1 chunk, sorted by cost (KV tiles x query tiles, descending) so
+//     that greedy claiming is longest-first.
+// Each list item stands for num_heads units, one per head.
+#include <atomic>
+
+#include "device_common.cuh"
+#include "kernels.h"
+#include "runtime.h"
+
+namespace cb {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kCostBuckets = 4096;     // costs at or above the last bucket share it
+constexpr int kUnitsPerCta = 6;        // decode units per persistent CTA the split size aims for
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Exclusive block-wide scan of 64-bit values (two 32-bit counters packed,
+// which add without carries between them).  Returns this thread's prefix;
+// `total` receives the block sum.  Contains __syncthreads.
+__device__ uint64_t block_excl_scan(uint64_t v, uint64_t* warp_sums, uint64_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    uint64_t w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) warp_sums[lane] = w;     // inclusive warp prefixes
+  }
+  __syncthreads();
+  total = warp_sums[(blockDim.x >> 5) - 1];
+  const uint64_t before = warp == 0 ? 0 : warp_sums[warp - 1];
+  const uint64_t r = before + x - v;
+  __syncthreads();                          // warp_sums is reused by the next call
+  return r;
+}
+
+// Prefill work of query pair qp of a chunk: KV tiles the pair streams times
+// the query tiles it holds.
+__device__ __forceinline__ int pair_cost(int q_len, int ctx, int qp) {
+  const int row0 = qp * kPrefillPairRows;
+  const int nq = row0 + kPrefillPairRows / 2 < q_len ? 2 : 1;
+  const int kv_end = min(ctx - q_len + row0 + nq * (kPrefillPairRows / 2), ctx);
+  return ((kv_end + 127) / 128) * nq;
+}
+
+struct RowInfo {
+  int q_len, ctx;
+  bool bad;
+};
+
+__device__ __forceinline__ RowInfo row_info(const AttnArgs& a, int s) {
+  RowInfo r;
+  const int c0 = a.cu_seqlens_q[s];
+  const int c1 = a.cu_seqlens_q[s + 1];
+  r.q_len = c1 - c0;
+  r.ctx = a.context_lens[s];
+  r.bad = r.q_len < 1 || r.ctx < r.q_len || r.ctx > a.max_context_len || r.q_len > a.max_q_len || c0 < 0 ||
+          c1 > a.num_tokens || (int64_t(r.ctx) + a.block_size - 1) / a.block_size > a.max_blocks_per_seq;
+  return r;
+}
+
+// Stable-enough counting sort of n items into `out`, largest key first (keys
+// at or above the last bucket share it).  Block-wide; contains __syncthreads.
+template <typename Key>
+__device__ void sort_desc(const int2* in, int2* out, int n, Key key, uint32_t* bucket, uint64_t* warp_sums) {
+  if (n <= 1) {
+    if (n == 1 && threadIdx.x == 0) out[0] = in[0];
+    return;
+  }
+  for (int i = threadIdx.x; i < kCostBuckets; i += kPlanThreads) bucket[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kPlanThreads) atomicAdd(&bucket[min(key(in[i]), kCostBuckets - 1)], 1u);
+  __syncthreads();
+  // descending order: thread t owns buckets kCostBuckets-1-4t .. kCostBuckets-4-4t
+  constexpr int kPer = kCostBuckets / kPlanThreads;
+  uint32_t local[kPer], sum = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    local[k] = bucket[kCostBuckets - 1 - (threadIdx.x * kPer + k)];
+    sum += local[k];
+  }
+  uint64_t total;
+  uint32_t run = uint32_t(block_excl_scan(sum, warp_sums, total));
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    bucket[kCostBuckets - 1 - (threadIdx.x * kPer + k)] = run;
+    run += local[k];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kPlanThreads) {
+    const int2 it = in[i];
+    out[atomicAdd(&bucket[min(key(it), kCostBuckets - 1)], 1u)] = it;
+  }
+  __syncthreads();                          // `bucket` is reused by the next sort
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs a, const StepPlan p) {
+  launch_dependents();                      // they wait for this grid on the device
+  __shared__ uint64_t warp_sums[32];
+  __shared__ uint32_t bucket[kCostBuckets];
+  const int tid = threadIdx.x;
+
+  // Pass 1: check every row; total keys of the decode rows.
+  uint64_t dec_keys = 0;
+  for (int s = tid; s < a.num_seqs; s += kPlanThreads) {
+    const RowInfo r = row_info(a, s);
+    if (r.bad)
+      raise_error(a.err, kErrInvalid);
+    else if (r.q_len == 1)
+      dec_keys += uint64_t(r.ctx);
+  }
+  uint64_t total_keys;
+  block_excl_scan(dec_keys, warp_sums, total_keys);
+  // Keys per decode split: every split pays a fixed cost (its merge and a
+  // partial result round trip), so splits are as long as possible while the
+  // decode grid still gets kUnitsPerCta units per CTA to balance over.
+  const uint64_t target = uint64_t(p.dec_ctas > 0 ? p.dec_ctas : 1) * kUnitsPerCta;
+  const uint64_t want = (total_keys * uint64_t(a.num_heads) + target - 1) / target;
+  const uint64_t per = want < uint64_t(kSplitKeys) ? uint64_t(kSplitKeys) : want;
+  const uint64_t rounded = (per + kSplitKeys - 1) / kSplitKeys * kSplitKeys;
+  const int split = rounded > (uint64_t(1) << 30) ? (1 << 30) : int(rounded);
+
+  // Pass 2: list the items (unsorted).
+  uint64_t base = 0;                        // items so far: decode in the low, prefill in the high word
+  for (int s0 = 0; s0 < a.num_seqs; s0 += kPlanThreads) {
+    const int s = s0 + tid;
+    uint32_t nd = 0, np = 0;
+    if (s < a.num_seqs) {
+      const RowInfo r = row_info(a, s);
+      if (!r.bad) {
+        if (r.q_len == 1)
+          nd = uint32_t((r.ctx + split - 1) / split);
+        else
+          np = uint32_t((r.q_len + kPrefillPairRows - 1) / kPrefillPairRows);
+      }
+    }
+    uint64_t total;
+    const uint64_t off = base + block_excl_scan(uint64_t(nd) | (uint64_t(np) << 32), warp_sums, total);
+    base += total;
+    const uint32_t od = uint32_t(off), op = uint32_t(off >> 32);
+    if (nd > 0) {
+      if (od + nd <= uint32_t(p.dec_cap)) {
+        for (uint32_t k = 0; k < nd; ++k) p.dec_scratch[od + k] = make_int2(s, int(k));
+      } else {
+        raise_error(a.err, kErrInvalid);
+      }
+    }
+    if (np > 0) {
+      if (op + np <= uint32_t(p.pre_cap)) {
+        for (uint32_t k = 0; k < np; ++k) p.pre_scratch[op + k] = make_int2(s, int(k));
+      } else {
+        raise_error(a.err, kErrInvalid);      // overlapping query ranges (malformed cu_seqlens_q)
+      }
+    }
+  }
+  const int n_dec = min(int(uint32_t(base)), p.dec_cap);
+  const int n_pre = min(int(uint32_t(base >> 32)), p.pre_cap);
+  // split tickets start at zero (coalesced over the whole [num_seqs][H] array)
+  for (int i = tid; i < a.num_seqs * a.num_heads; i += kPlanThreads) p.tickets[i] = 0;
+  __syncthreads();                          // every thread's items are written before any is re-read
+
+  // Longest first, so that greedy claiming ends on short units.
+  sort_desc(p.dec_scratch, p.dec_items, n_dec,
+            [&](int2 it) {
+              const int len = min(a.context_lens[it.x] - it.y * split, split);
+              return (len + 15) / 16;
+            },
+            bucket, warp_sums);
+  sort_desc(p.pre_scratch, p.pre_items, n_pre,
+            [&](int2 it) {
+              const int q_len = a.cu_seqlens_q[it.x + 1] - a.cu_seqlens_q[it.x];
+              return pair_cost(q_len, a.context_lens[it.x], it.y);
+            },
+            bucket, warp_sums);
+  if (tid == 0) {
+    p.header[0] = n_dec;
+    p.header[1] = n_pre;
+    p.header[2] = 0;
+    p.header[3] = 0;
+    p.header[4] = int32_t(p.tag);
+    p.header[5] = split;
+  }
+}
+
+}  // namespace
+
+size_t step_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_heads, int32_t head_dim,
+                            int32_t max_context_len) {
+  const size_t S = size_t(num_seqs > 0 ? num_seqs : 0), T = size_t(num_tokens > 0 ? num_tokens : 0);
+  const size_t splits = size_t((max_context_len + kSplitKeys - 1) / kSplitKeys);
+  const size_t pre_cap = T / kPrefillPairRows + (S < T / 2 ? S : T / 2) + 1;
+  return 256 +                                                        // header
+         2 * align256(S * splits * sizeof(int2)) +                    // decode items + scratch
+         2 * align256(pre_cap * sizeof(int2)) +                       // prefill items + scratch
+         align256(S * num_heads * sizeof(int32_t)) +                  // tickets
+         (splits > 1 ? S * num_heads * splits * (head_dim + 2) * sizeof(float) : 0);   // partials
+}
+
+cb_status step_plan_layout(void* workspace, size_t workspace_bytes, int32_t num_seqs, int32_t num_tokens,
+                           int32_t num_heads, int32_t head_dim, int32_t max_context_len, StepPlan* plan) {
+  const size_t need = step_workspace_bytes(num_seqs, num_tokens, num_heads, head_dim, max_context_len);
+  if (!workspace || workspace_bytes < need)
+    return fail(CB_ERR_INVALID, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(CB_ERR_INVALID, "workspace must be 256-byte aligned");
+  const size_t S = size_t(num_seqs), T = size_t(num_tokens);
+  const size_t splits = size_t((max_context_len + kSplitKeys - 1) / kSplitKeys);
+  const size_t pre_cap = T / kPrefillPairRows + (S < T / 2 ? S : T / 2) + 1;
+  char* w = static_cast<char*>(workspace);
+  plan->header = reinterpret_cast<int32_t*>(w);
+  w += 256;
+  plan->dec_items = reinterpret_cast<int2*>(w);
+  w += align256(S * splits * sizeof(int2));
+  plan->dec_scratch = reinterpret_cast<int2*>(w);
+  w += align256(S * splits * sizeof(int2));
+  plan->pre_items = reinterpret_cast<int2*>(w);
+  w += align256(pre_cap * sizeof(int2));
+  plan->pre_scratch = reinterpret_cast<int2*>(w);
+  w += align256(pre_cap * sizeof(int2));
+  plan->tickets = reinterpret_cast<int32_t*>(w);
+  w += align256(S * num_heads * sizeof(int32_t));
+  plan->partials = reinterpret_cast<float*>(w);
+  plan->max_splits = int32_t(splits);
+  plan->dec_cap = int32_t(S * splits);
+  plan->pre_cap = int32_t(pre_cap);
+  plan->dec_ctas = 0;
+  static std::atomic<uint32_t> next_tag{1};
+  plan->tag = next_tag.fetch_add(1);
+  return CB_OK;
+}
+
+cb_status launch_plan(const AttnArgs& a, const StepPlan& plan, cudaStream_t stream) {
+  plan_step_kernel<<<1, kPlanThreads, 0, stream>>>(a, plan);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "step plan: launch");
+  return CB_OK;
+}
+
+}  // namespace cb

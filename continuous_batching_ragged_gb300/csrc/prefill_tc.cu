@@ -40,6 +40,8 @@
 //     stores its row.
 // Every wait is bounded; a timeout sets the device error word and the CTA
 // winds down, freeing its TMEM.
+#include <algorithm>
+
 #include <cuda.h>
 
 #include "device_common.cuh"
@@ -68,9 +70,12 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQTiles * kTile;
 constexpr uint32_t kOffV = kOffK + kKStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
+constexpr int kItemSlots = 2;                    // claimed work items in flight
+constexpr int kItemReaders = 1 + 1 + 8;          // V loader, MMA, softmax warps (one arrival each)
 enum : int {
-  BAR_Q = 0,
-  BAR_S = 1,                   // + t: S_t ready
+  BAR_Q = 0,                   // Q tiles landed
+  BAR_QE = 1,                  // every S MMA of the unit has read Q
+  BAR_S = 2,                   // + t: S_t ready
   BAR_P = BAR_S + kQTiles,     // + t: P_t written (128 arrivals)
   BAR_O = BAR_P + kQTiles,     // + t: P_t V done
   BAR_KF = BAR_O + kQTiles,    // + stage: K landed
@@ -78,12 +83,16 @@ enum : int {
   BAR_VF = BAR_KE + kKStages,  // + stage: V landed (and its tail zeroed)
   BAR_VE = BAR_VF + kVStages,  // + stage: V consumed
   BAR_VTAIL = BAR_VE + kVStages,
-  NUM_BARS = BAR_VTAIL + 1
+  BAR_IF = BAR_VTAIL + 1,      // + slot: work item published
+  BAR_IE = BAR_IF + kItemSlots,  // + slot: work item read by every role
+  BAR_DONE = BAR_IE + kItemSlots,  // the MMA thread's last MMAs completed
+  NUM_BARS = BAR_DONE + 1
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + 8 * NUM_BARS;
+constexpr uint32_t kOffItems = kOffTmemSlot + 16;  // kItemSlots work items of 32 bytes
 constexpr int kLookAhead = 4;                    // tiles of block-table look-ahead and L2 prefetch
 constexpr int kRing = 8;                         // box-index ring slots per loader (> kLookAhead)
-constexpr uint32_t kOffRing = kOffTmemSlot + 16; // two rings (K, V) of kRing x 16 ints
+constexpr uint32_t kOffRing = kOffItems + kItemSlots * 32;  // two rings (K, V) of kRing x 16 ints
 constexpr uint32_t kSmemBytes = kOffRing + 2 * kRing * 16 * 4 + 1024;   // + slack to align the base
 static_assert(kRing > kLookAhead, "ring must outlive the look-ahead");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -163,42 +172,60 @@ __device__ __forceinline__ void load_kv_tile_ring(uint32_t dst, const CUtensorMa
   }
 }
 
+// One claimed unit of work: a 256-row query pair of one chunk, one head.
+struct WorkItem {
+  int u;                                           // unit index; >= the unit count: no more work
+  int s, h, row0, c0, q_len, ctx, pad;
+};
+static_assert(sizeof(WorkItem) == 32, "work item slot");
+
+// Shape of a unit: query tiles holding real rows, KV tiles any row can see.
+struct UnitShape {
+  int nq, p, n_tiles;
+};
+__device__ __forceinline__ UnitShape unit_shape(const WorkItem& it) {
+  UnitShape sh;
+  sh.nq = it.row0 + BM < it.q_len ? 2 : 1;
+  sh.p = it.ctx - it.q_len;                        // cached tokens before this step
+  const int kv_end = min(sh.p + it.row0 + sh.nq * BM, it.ctx);
+  sh.n_tiles = (kv_end + BN - 1) / BN;
+  return sh;
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+struct PrefillWork {
+  const int2* items;        // the plan's (sequence, query pair) items, costliest first
+  const int32_t* header;    // [1] = number of items
+  int32_t* claims;          // claim counter
+  int32_t item_cap;         // capacity of the item list
+  uint32_t tag;             // the plan's call tag
+};
+
+// Persistent: a fixed grid of CTAs (one per SM) claims units until none are
+// left.  The K loader claims each unit and publishes it in a two-slot ring of
+// work items that the V loader, the MMA thread and the softmax warps read in
+// the same order; every barrier phase runs on across units, so the next
+// unit's K tiles and Q load overlap the end of the current one.
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
-  const int qp = gridDim.x - 1 - blockIdx.x;       // the longest tile pairs launch first
-  const int h = blockIdx.y;
-  const int s = blockIdx.z;
-  const int c0 = a.cu_seqlens_q[s];
-  const int c1 = a.cu_seqlens_q[s + 1];
-  const int q_len = c1 - c0;
-  if (q_len == 1) return;                          // a decode row: the split-KV kernel's
-  const int ctx = a.context_lens[s];
-  const int B = a.block_size;
-  const bool bad = q_len < 1 || ctx < q_len || ctx > a.max_context_len || q_len > a.max_q_len ||
-                   c0 < 0 || c1 > a.num_tokens || (ctx + B - 1) / B > a.max_blocks_per_seq;
-  if (bad) {
-    if (qp == 0 && h == 0 && threadIdx.x == 0) raise_error(a.err, kErrInvalid);
-    return;
-  }
-  const int row0 = qp * kQTiles * BM;             // first chunk row of tile 0
-  if (row0 >= q_len) return;
-  const int nq = row0 + BM < q_len ? 2 : 1;        // tiles of this pair holding real rows
-  const int p = ctx - q_len;                       // cached tokens before this step
-  const int kv_end = min(p + row0 + nq * BM, ctx); // keys any row of the pair can see
-  const int n_tiles = (kv_end + BN - 1) / BN;
-
+                      const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const PrefillWork w) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;    // 128B-swizzled tiles need 1 KB alignment
   uint8_t* gsm = smem_raw + (base - raw);
   auto bar = [&](int i) -> uint32_t { return base + kOffBar + 8u * uint32_t(i); };
+  WorkItem* items = reinterpret_cast<WorkItem*>(gsm + kOffItems);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int32_t* bt = a.block_tables + size_t(s) * a.max_blocks_per_seq;
+  const int B = a.block_size;
+  const int H = a.num_heads;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
+    mbar_init(bar(BAR_QE), 1);
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(bar(BAR_S + t), 1);
       mbar_init(bar(BAR_P + t), BM);
@@ -213,6 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(BAR_VE + st), 1);
     }
     mbar_init(bar(BAR_VTAIL), 1);
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(bar(BAR_IF + i), 1);
+      mbar_init(bar(BAR_IE + i), kItemReaders);
+    }
+    mbar_init(bar(BAR_DONE), 1);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -222,79 +254,195 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gsm + kOffTmemSlot);
+  grid_dependency_wait();                          // the plan kernel has finished
+  const uint32_t seen_tag = uint32_t(__ldcg(w.header + 4));
+  int n_items = __ldcg(w.header + 1);
+  if (seen_tag != w.tag || n_items < 0 || n_items > w.item_cap) {   // a list from another call: no work
+    if (threadIdx.x == 0) raise_error(a.err, kErrInvalid);
+    n_items = 0;
+  }
+  const int n_units = n_items * H;
+
+  // A reader's view of work item n: wait for it, copy it, release the slot.
+  // `arrive`: this thread is its warp's (or role's) one arrival.
+  auto read_item = [&](int n, bool arrive, WorkItem& it) -> bool {
+    const int slot = n % kItemSlots;
+    if (!mbar_wait(bar(BAR_IF + slot), (n / kItemSlots) & 1)) return false;
+    it = items[slot];
+    if (arrive) mbar_arrive(bar(BAR_IE + slot));
+    return true;
+  };
 
   if (warp == kWarpK) {
-    // ------------------------------------------------------------ K loader
+    // ------------------------------------------------------------ K loader (claims the work)
     int* ring = reinterpret_cast<int*>(gsm + kOffRing);
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      mbar_arrive_expect_tx(bar(BAR_Q), kQTiles * kTile);
-      for (int t = 0; t < kQTiles; ++t) {
-        tma_load_3d(base + kOffQ + t * kTile, &tm_q, bar(BAR_Q), 0, h, c0 + row0 + t * BM);
-        tma_load_3d(base + kOffQ + t * kTile + kHalf, &tm_q, bar(BAR_Q), 64, h, c0 + row0 + t * BM);
-      }
     }
-    for (int j = 0; j < min(kLookAhead, n_tiles); ++j) stage_boxes(j, B, ctx, bt, a, h, lane, ring, &tm_k);
-    for (int j = 0; j < n_tiles; ++j) {
-      if (j + kLookAhead < n_tiles) stage_boxes(j + kLookAhead, B, ctx, bt, a, h, lane, ring, &tm_k);
-      const int st = j % kKStages;
-      if (j >= kKStages && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_KE + st), ((j / kKStages) - 1) & 1))) {
-        if (lane == 0) raise_error(a.err, kErrTimeout);
+    uint32_t kc = 0;                               // K tiles issued so far
+    int n = 0;                                     // units claimed so far
+    bool ok = true;
+    unsigned site = 0;
+    for (;; ++n) {
+      const int slot = n % kItemSlots;
+      if (n >= kItemSlots &&
+          !__all_sync(0xffffffffu, mbar_wait(bar(BAR_IE + slot), ((n / kItemSlots) - 1) & 1))) {
+        ok = false;
+        site = kSitePfItemFree;
         break;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(BAR_KF + st), kTile);
-        load_kv_tile_ring(base + kOffK + st * kTile, &tm_k, bar(BAR_KF + st), B, ring + (j % kRing) * 16);
+        WorkItem it = {};
+        it.u = atomicAdd(w.claims, 1);
+        if (it.u < n_units) {
+          const int2 pi = __ldcg(w.items + it.u / H);
+          it.s = pi.x;
+          it.h = it.u % H;
+          it.row0 = pi.y * kPrefillPairRows;
+          bool bad = it.s < 0 || it.s >= a.num_seqs || pi.y < 0;
+          if (!bad) {
+            it.c0 = __ldcg(a.cu_seqlens_q + it.s);
+            it.q_len = __ldcg(a.cu_seqlens_q + it.s + 1) - it.c0;
+            it.ctx = __ldcg(a.context_lens + it.s);
+            bad = it.c0 < 0 || it.q_len < 2 || it.c0 + it.q_len > a.num_tokens || it.row0 >= it.q_len ||
+                  it.ctx < it.q_len || it.ctx > a.max_context_len;
+          }
+          if (bad) {                               // never happens with a plan from this call
+            raise_error(a.err, kErrInvalid);
+            it.u = n_units;
+          }
+        }
+        items[slot] = it;
+        mbar_arrive(bar(BAR_IF + slot));         // release: the slot's contents are visible
       }
       __syncwarp();
+      const WorkItem it = items[slot];
+      if (it.u >= n_units) break;
+      const UnitShape sh = unit_shape(it);
+      const int32_t* bt = a.block_tables + size_t(it.s) * a.max_blocks_per_seq;
+      // Q of this unit goes in once every S MMA of the previous unit has read
+      // the old Q; the first K tiles are requested before that wait.
+      auto load_q = [&]() -> bool {
+        if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_QE), (n - 1) & 1))) return false;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(BAR_Q), kQTiles * kTile);
+          for (int t = 0; t < kQTiles; ++t) {
+            const int row = it.c0 + it.row0 + t * BM;
+            tma_load_3d(base + kOffQ + t * kTile, &tm_q, bar(BAR_Q), 0, it.h, row);
+            tma_load_3d(base + kOffQ + t * kTile + kHalf, &tm_q, bar(BAR_Q), 64, it.h, row);
+          }
+        }
+        __syncwarp();
+        return true;
+      };
+      const int q_at = min(kKStages - 1, sh.n_tiles);   // K tiles requested before the Q load
+      for (int j = 0; j < min(kLookAhead, sh.n_tiles); ++j)
+        stage_boxes(j, B, it.ctx, bt, a, it.h, lane, ring, &tm_k);
+      for (int j = 0; j < sh.n_tiles; ++j) {
+        if (j == q_at && !load_q()) {
+          ok = false;
+          site = kSitePfQFree;
+          break;
+        }
+        if (j + kLookAhead < sh.n_tiles) stage_boxes(j + kLookAhead, B, it.ctx, bt, a, it.h, lane, ring, &tm_k);
+        const uint32_t g = kc + j;
+        const int st = g % kKStages;
+        if (g >= kKStages && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_KE + st), ((g / kKStages) - 1) & 1))) {
+          ok = false;
+          site = kSitePfKFree;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(BAR_KF + st), kTile);
+          load_kv_tile_ring(base + kOffK + st * kTile, &tm_k, bar(BAR_KF + st), B, ring + (j % kRing) * 16);
+        }
+        __syncwarp();
+      }
+      if (ok && q_at == sh.n_tiles && !load_q()) {
+        ok = false;
+        site = kSitePfQFree;
+      }
+      if (!ok) break;
+      kc += sh.n_tiles;
+    }
+    if (!ok && lane == 0) raise_error(a.err, kErrTimeout | site);
+    if (lane == 0) {
+      // (error path) let copies still in flight land before the CTA exits
+      for (uint32_t g = kc > uint32_t(kKStages) ? kc - kKStages : 0; g < kc; ++g)
+        mbar_wait(bar(BAR_KF + g % kKStages), (g / kKStages) & 1);
+      if (n > 0) mbar_wait(bar(BAR_Q), (n - 1) & 1);
     }
   } else if (warp == kWarpV) {
     // ------------------------------------------------------------ V loader
     int* ring = reinterpret_cast<int*>(gsm + kOffRing) + kRing * 16;
     if (lane == 0) tma_prefetch_desc(&tm_v);
-    for (int j = 0; j < min(kLookAhead, n_tiles); ++j) stage_boxes(j, B, ctx, bt, a, h, lane, ring, &tm_v);
-    for (int j = 0; j < n_tiles; ++j) {
-      if (j + kLookAhead < n_tiles) stage_boxes(j + kLookAhead, B, ctx, bt, a, h, lane, ring, &tm_v);
-      const int st = j % kVStages;
-      if (j >= kVStages && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_VE + st), ((j / kVStages) - 1) & 1))) {
-        if (lane == 0) raise_error(a.err, kErrTimeout);
+    uint32_t vc = 0, vtail = 0;                    // V tiles issued, tail fix-ups done
+    bool ok = true;
+    unsigned site = 0;
+    for (int n = 0;; ++n) {
+      WorkItem it;
+      if (!__all_sync(0xffffffffu, read_item(n, false, it))) {
+        ok = false;
+        site = kSitePfItem;
         break;
       }
-      const int kb = j * BN;
-      const int r0 = ctx - kb;                               // first row past the context
-      const int r1 = min(BN, ((ctx + B - 1) / B) * B - kb);  // end of the last paged block
-      const bool tail = j == n_tiles - 1 && r0 < r1;
-      const uint32_t vdst = base + kOffV + st * kTile;
-      if (lane == 0) {
-        const uint32_t land = tail ? bar(BAR_VTAIL) : bar(BAR_VF + st);
-        mbar_arrive_expect_tx(land, kTile);
-        load_kv_tile_ring(vdst, &tm_v, land, B, ring + (j % kRing) * 16);
-      }
       __syncwarp();
-      if (tail) {
-        // zero the stale rows of the last paged block, then publish the tile
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_VTAIL), 0))) {
-          if (lane == 0) raise_error(a.err, kErrTimeout);
+      if (lane == 0) mbar_arrive(bar(BAR_IE + n % kItemSlots));
+      if (it.u >= n_units) break;
+      const UnitShape sh = unit_shape(it);
+      const int32_t* bt = a.block_tables + size_t(it.s) * a.max_blocks_per_seq;
+      for (int j = 0; j < min(kLookAhead, sh.n_tiles); ++j)
+        stage_boxes(j, B, it.ctx, bt, a, it.h, lane, ring, &tm_v);
+      for (int j = 0; j < sh.n_tiles; ++j) {
+        if (j + kLookAhead < sh.n_tiles) stage_boxes(j + kLookAhead, B, it.ctx, bt, a, it.h, lane, ring, &tm_v);
+        const uint32_t g = vc + j;
+        const int st = g % kVStages;
+        if (g >= kVStages && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_VE + st), ((g / kVStages) - 1) & 1))) {
+          ok = false;
+          site = kSitePfVFree;
           break;
         }
-        uint8_t* vt = gsm + kOffV + st * kTile;
-        for (int c = lane; c < (r1 - r0) * 16; c += 32) {
-          const int r = r0 + c / 16, w = c % 16;
-          *reinterpret_cast<uint4*>(vt + (w / 8) * kHalf + r * 128 + (w % 8) * 16) = make_uint4(0, 0, 0, 0);
+        const int kb = j * BN;
+        const int r0 = it.ctx - kb;                                // first row past the context
+        const int r1 = min(BN, ((it.ctx + B - 1) / B) * B - kb);   // end of the last paged block
+        const bool tail = j == sh.n_tiles - 1 && r0 < r1;
+        const uint32_t vdst = base + kOffV + st * kTile;
+        if (lane == 0) {
+          const uint32_t land = tail ? bar(BAR_VTAIL) : bar(BAR_VF + st);
+          mbar_arrive_expect_tx(land, kTile);
+          load_kv_tile_ring(vdst, &tm_v, land, B, ring + (j % kRing) * 16);
         }
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_VF + st));
+        if (tail) {
+          // zero the stale rows of the last paged block, then publish the tile
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_VTAIL), vtail & 1))) {
+            ok = false;
+            site = kSitePfVTail;
+            break;
+          }
+          ++vtail;
+          uint8_t* vt = gsm + kOffV + st * kTile;
+          for (int c = lane; c < (r1 - r0) * 16; c += 32) {
+            const int r = r0 + c / 16, wd = c % 16;
+            *reinterpret_cast<uint4*>(vt + (wd / 8) * kHalf + r * 128 + (wd % 8) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(BAR_VF + st));
+        }
       }
+      if (!ok) break;
+      vc += sh.n_tiles;
     }
+    if (!ok && lane == 0) raise_error(a.err, kErrTimeout | site);
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);   // Q (K-major) x K (K-major)
       constexpr uint32_t idO = idesc_bf16_f32(BM, HD, true);    // P (TMEM) x V (N-contiguous)
-      auto issue_s = [&](int t, int x) {
-        const uint32_t kb = base + kOffK + (x % kKStages) * kTile;
+      auto issue_s = [&](int t, uint32_t g) {
+        const uint32_t kb = base + kOffK + (g % kKStages) * kTile;
         const uint32_t qb = base + kOffQ + t * kTile;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
@@ -303,165 +451,217 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar(BAR_S + t));
       };
-      auto issue_pv = [&](int t, int x) {
-        const uint32_t vb = base + kOffV + (x % kVStages) * kTile;
+      auto issue_pv = [&](int t, uint32_t g, bool accumulate) {
+        const uint32_t vb = base + kOffV + (g % kVStages) * kTile;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
           mma_f16_ts(tmem + 256 * t + 128, tmem + 256 * t + k * 8, smem_desc(vb + k * 2048, kHalf, 1024), idO,
-                     (x > 0 || k > 0));
+                     accumulate || k > 0);
         mma_commit(bar(BAR_O + t));
       };
       // Fixed issue order per KV tile j: P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1).
       // S_t(j+1) overwrites the TMEM columns that P_t V_j reads; tcgen05.mma
       // ops issued by one thread execute in issue order, so the read comes
       // first.  While the softmax of one tile runs, the tensor core works
-      // through the other tile's P V and next S.
-      bool ok = mbar_wait(bar(BAR_Q), 0) && mbar_wait(bar(BAR_KF), 0);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < nq; ++t) issue_s(t, 0);
-        mma_commit(bar(BAR_KE));
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const bool next = j + 1 < n_tiles;
-        if (!mbar_wait(bar(BAR_VF + j % kVStages), (j / kVStages) & 1)) {
+      // through the other tile's P V and next S.  The first S of the next
+      // unit follows the last P V of this one the same way.
+      uint32_t kc = 0, vc = 0, cnt0 = 0, cnt1 = 0;  // K, V tiles consumed; S/P/O phases of tiles 0, 1
+      bool ok = true;
+      unsigned site = 0;
+      for (int n = 0; ok; ++n) {
+        WorkItem it;
+        if (!read_item(n, true, it)) {
           ok = false;
+          site = kSitePfItem;
           break;
         }
-        for (int t = 0; t < nq; ++t) {
-          if (!mbar_wait(bar(BAR_P + t), j & 1)) {
+        if (it.u >= n_units) break;
+        const UnitShape sh = unit_shape(it);
+        if (!mbar_wait(bar(BAR_Q), n & 1)) {
+          ok = false;
+          site = kSitePfQ;
+          break;
+        }
+        if (!mbar_wait(bar(BAR_KF + kc % kKStages), (kc / kKStages) & 1)) {
+          ok = false;
+          site = kSitePfK;
+          break;
+        }
+        tc_fence_after();
+        for (int t = 0; t < sh.nq; ++t) issue_s(t, kc);
+        mma_commit(bar(BAR_KE + kc % kKStages));
+        if (sh.n_tiles == 1) mma_commit(bar(BAR_QE));
+        for (int j = 0; ok && j < sh.n_tiles; ++j) {
+          const bool next = j + 1 < sh.n_tiles;
+          const uint32_t gv = vc + j, gk = kc + j + 1;
+          if (!mbar_wait(bar(BAR_VF + gv % kVStages), (gv / kVStages) & 1)) {
             ok = false;
+            site = kSitePfV;
             break;
           }
-          tc_fence_after();
-          issue_pv(t, j);
-          if (t == nq - 1) mma_commit(bar(BAR_VE + j % kVStages));          // both read V_j
-          if (next) {
-            if (t == 0 && !mbar_wait(bar(BAR_KF + (j + 1) % kKStages), ((j + 1) / kKStages) & 1)) {
+          for (int t = 0; t < sh.nq; ++t) {
+            if (!mbar_wait(bar(BAR_P + t), ((t == 0 ? cnt0 : cnt1) + j) & 1)) {
               ok = false;
+              site = kSitePfP;
               break;
             }
             tc_fence_after();
-            issue_s(t, j + 1);
-            if (t == nq - 1) mma_commit(bar(BAR_KE + (j + 1) % kKStages));  // both read K_{j+1}
+            issue_pv(t, gv, j > 0);
+            if (t == sh.nq - 1) mma_commit(bar(BAR_VE + gv % kVStages));        // both read V_j
+            if (next) {
+              if (t == 0 && !mbar_wait(bar(BAR_KF + gk % kKStages), (gk / kKStages) & 1)) {
+                ok = false;
+                site = kSitePfK;
+                break;
+              }
+              tc_fence_after();
+              issue_s(t, gk);
+              if (t == sh.nq - 1) {
+                mma_commit(bar(BAR_KE + gk % kKStages));                       // both read K_{j+1}
+                if (j + 2 == sh.n_tiles) mma_commit(bar(BAR_QE));              // the unit's last S
+              }
+            }
           }
         }
+        kc += sh.n_tiles;
+        vc += sh.n_tiles;
+        cnt0 += sh.n_tiles;
+        if (sh.nq > 1) cnt1 += sh.n_tiles;
       }
-      if (!ok) raise_error(a.err, kErrTimeout);
+      if (!ok) raise_error(a.err, kErrTimeout | site);
+      mma_commit(bar(BAR_DONE));                   // every MMA issued so far has completed
+      mbar_wait(bar(BAR_DONE), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;                       // query tile of this warpgroup
     const int wq = warp & 3;                       // TMEM lane quarter
     const int i = threadIdx.x - BM * t;            // tile row = TMEM lane
-    const int qi = row0 + BM * t + i;              // row within the chunk
-    const int limit = min(p + qi, ctx - 1);        // last key this row sees
-    const int warp_limit = min(p + row0 + BM * t + 32 * wq, ctx - 1);   // smallest in the warp
     const uint32_t lane_base = tmem + (uint32_t(wq * 32) << 16) + 256 * t;
     const float sl2 = a.scale_log2;
-    float m = -INFINITY, l = 0.f;
-    bool ok = t < nq;
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      if (!mbar_wait(bar(BAR_S + t), j & 1)) {
+    uint32_t cnt = 0;                              // S/O phases of this tile consumed
+    bool ok = true;
+    unsigned site = 0;
+    for (int n = 0; ok; ++n) {
+      WorkItem it;
+      if (!__all_sync(0xffffffffu, read_item(n, false, it))) {
         ok = false;
+        site = kSitePfItem;
         break;
       }
-      tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld128(lane_base, sr);
-      tmem_wait_ld();
-      const int kb = j * BN;
-      float mt = -INFINITY;
-      if (kb + BN - 1 > warp_limit) {              // the tile crosses some row's diagonal: mask
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (kb + c > limit) sr[c] = __float_as_uint(-INFINITY);
-      }
-      {                                            // four independent max chains (latency, not issue, bound)
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < BN; c += 8)
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            m4[u] = max3(m4[u], __uint_as_float(sr[c + 2 * u]), __uint_as_float(sr[c + 2 * u + 1]));
-        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      }
-      const float m_new = fmaxf(m, mt * sl2);
-      const bool resc = m_new > m + 8.0f;         // keep a stale max while exp2 stays <= 2^8
-      const float m_use = resc ? m_new : m;
-      const float alpha = resc ? ex2(m - m_new) : 1.0f;
-      const uint64_t scale2 = f2_pack(sl2, sl2);
-      const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
-      uint64_t sum2[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {               // P packed in place over the scores
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), scale2, neg_m2),
-                  x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        sum2[c & 3] = f2_add(sum2[c & 3], f2_pack(p0, p1));
-        sr[c] = pack_bf16x2(p0, p1);
-      }
-      float rs0, rs1, rs2, rs3, rs4, rs5, rs6, rs7;
-      f2_unpack(sum2[0], rs0, rs1);
-      f2_unpack(sum2[1], rs2, rs3);
-      f2_unpack(sum2[2], rs4, rs5);
-      f2_unpack(sum2[3], rs6, rs7);
-      const float rs = ((rs0 + rs1) + (rs2 + rs3)) + ((rs4 + rs5) + (rs6 + rs7));
-      l = l * alpha + rs;
-      m = m_use;
-      tc_fence_before();
-      if (j > 0) {                                 // P_t V of tile j-1 done: O_t stable
-        if (!mbar_wait(bar(BAR_O + t), (j - 1) & 1)) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_IE + n % kItemSlots));
+      if (it.u >= n_units) break;
+      const UnitShape sh = unit_shape(it);
+      if (t >= sh.nq) continue;                    // this tile holds no rows of the unit
+      const int qi = it.row0 + BM * t + i;         // row within the chunk
+      const int limit = min(sh.p + qi, it.ctx - 1);  // last key this row sees
+      const int warp_limit = min(sh.p + it.row0 + BM * t + 32 * wq, it.ctx - 1);   // smallest in the warp
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; ok && j < sh.n_tiles; ++j) {
+        if (!mbar_wait(bar(BAR_S + t), (cnt + j) & 1)) {
           ok = false;
+          site = kSitePfS;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
+        uint32_t sr[128];
+        tmem_ld128(lane_base, sr);
+        tmem_wait_ld();
+        const int kb = j * BN;
+        float mt = -INFINITY;
+        if (kb + BN - 1 > warp_limit) {            // the tile crosses some row's diagonal: mask
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + 128 + 32 * c, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(lane_base + 128 + 32 * c, o);
-          }
+          for (int c = 0; c < BN; ++c)
+            if (kb + c > limit) sr[c] = __float_as_uint(-INFINITY);
         }
-      }
-      tmem_st32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_st32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(BAR_P + t));
-    }
-    if (ok) {
-      if (mbar_wait(bar(BAR_O + t), (n_tiles - 1) & 1)) {
-        tc_fence_after();
-        const float inv = 1.0f / l;
-        __nv_bfloat16* dst =
-            static_cast<__nv_bfloat16*>(a.out) + (size_t(c0 + qi) * a.num_heads + h) * HD;
+        {                                          // four independent max chains (latency, not issue, bound)
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + 128 + 32 * c, o);
-          tmem_wait_ld();
-          if (qi < q_len) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+          for (int c = 0; c < BN; c += 8)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float* f = reinterpret_cast<const float*>(&o[8 * e]);
-              d4[e] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
-                                 pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+            for (int u = 0; u < 4; ++u)
+              m4[u] = max3(m4[u], __uint_as_float(sr[c + 2 * u]), __uint_as_float(sr[c + 2 * u + 1]));
+          mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        }
+        const float m_new = fmaxf(m, mt * sl2);
+        const bool resc = m_new > m + 8.0f;       // keep a stale max while exp2 stays <= 2^8
+        const float m_use = resc ? m_new : m;
+        const float alpha = resc ? ex2(m - m_new) : 1.0f;
+        const uint64_t scale2 = f2_pack(sl2, sl2);
+        const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
+        uint64_t sum2[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {             // P packed in place over the scores
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), scale2, neg_m2),
+                    x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          sum2[c & 3] = f2_add(sum2[c & 3], f2_pack(p0, p1));
+          sr[c] = pack_bf16x2(p0, p1);
+        }
+        float rs0, rs1, rs2, rs3, rs4, rs5, rs6, rs7;
+        f2_unpack(sum2[0], rs0, rs1);
+        f2_unpack(sum2[1], rs2, rs3);
+        f2_unpack(sum2[2], rs4, rs5);
+        f2_unpack(sum2[3], rs6, rs7);
+        const float rs = ((rs0 + rs1) + (rs2 + rs3)) + ((rs4 + rs5) + (rs6 + rs7));
+        l = l * alpha + rs;
+        m = m_use;
+        tc_fence_before();
+        if (j > 0) {                               // P_t V of tile j-1 done: O_t stable
+          if (!mbar_wait(bar(BAR_O + t), (cnt + j - 1) & 1)) {
+            ok = false;
+            site = kSitePfO;
+            break;
+          }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[32];
+              tmem_ld32(lane_base + 128 + 32 * c, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(lane_base + 128 + 32 * c, o);
             }
           }
         }
-      } else if (lane == 0) {
-        raise_error(a.err, kErrTimeout);
+        tmem_st32(lane_base, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_st32(lane_base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(BAR_P + t));
       }
-    } else if (t < nq && lane == 0) {
-      raise_error(a.err, kErrTimeout);
+      if (!ok) break;
+      if (!mbar_wait(bar(BAR_O + t), (cnt + sh.n_tiles - 1) & 1)) {
+        ok = false;
+        site = kSitePfO;
+        break;
+      }
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + (size_t(it.c0 + qi) * H + it.h) * HD;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + 128 + 32 * c, o);
+        tmem_wait_ld();
+        if (qi < it.q_len) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float* f = reinterpret_cast<const float*>(&o[8 * e]);
+            d4[e] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                               pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+          }
+        }
+      }
+      tc_fence_before();                           // O read before the next unit's first P V overwrites it
+      cnt += sh.n_tiles;
     }
+    if (!ok && lane == 0) raise_error(a.err, kErrTimeout | site);
   }
   tc_fence_before();
   __syncthreads();
@@ -476,14 +676,12 @@ bool g_attr_set[64] = {};
 
 }  // namespace
 
-cb_status launch_prefill_tc(const AttnArgs& a, cudaStream_t stream) {
+cb_status launch_prefill_tc(const AttnArgs& a, const StepPlan& plan, bool after_plan, cudaStream_t stream) {
   if (a.dtype != CB_DTYPE_BF16 || a.head_dim != HD)
     return fail(CB_ERR_UNSUPPORTED, "prefill chunks: bf16 with head_dim 128 only");
   const int B = a.block_size;
   if (B < 8 || B > BN || (B & (B - 1)) != 0)
     return fail(CB_ERR_UNSUPPORTED, "prefill chunks: block_size must be a power of two in [8, 128]");
-  if (a.num_seqs > 65535 || a.num_heads > 65535)
-    return fail(CB_ERR_UNSUPPORTED, "prefill chunks: more than 65535 sequences or heads");
   if (int64_t(a.num_blocks) * a.num_heads >= (int64_t(1) << 31))
     return fail(CB_ERR_UNSUPPORTED, "prefill chunks: num_blocks * num_heads must fit in int32");
   EncodeTiledFn enc = encode_tiled_fn();
@@ -520,11 +718,18 @@ cb_status launch_prefill_tc(const AttnArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "prefill chunks: shared memory attribute");
     g_attr_set[dev] = true;
   }
-  const int rows_per_cta = kQTiles * BM;
-  const dim3 grid(unsigned((a.max_q_len + rows_per_cta - 1) / rows_per_cta), unsigned(a.num_heads),
-                  unsigned(a.num_seqs));
-  prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, a);
-  cudaError_t e = cudaGetLastError();
+  PrefillWork w;
+  w.items = plan.pre_items;
+  w.header = plan.header;
+  w.claims = plan.header + 3;
+  w.item_cap = plan.pre_cap;
+  w.tag = plan.tag;
+  // one CTA per SM, never more than units could exist
+  const int64_t max_units = int64_t(plan.pre_cap) * a.num_heads;
+  const int64_t grid = std::min<int64_t>(sm_count(), max_units);
+  if (grid < 1) return CB_OK;
+  cudaError_t e = launch_kernel(prefill_tc_kernel, dim3(unsigned(grid)), dim3(kThreads), kSmemBytes, stream,
+                                after_plan, tq, tk, tv, a, w);
   if (e != cudaSuccess) return cuda_fail(e, "prefill chunks: launch");
   return CB_OK;
 }

@@ -135,7 +135,8 @@ extern "C" cb_status cb_check_device_errors(void* stream) {
   const unsigned zero = 0;
   e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
   if (e != cudaSuccess) return cb::cuda_fail(e, "cb_check_device_errors: clear error word");
-  if (word & cb::kErrTimeout) return cb::fail(CB_ERR_TIMEOUT, "a bounded device wait ran out");
+  if (word & cb::kErrTimeout)
+    return cb::fail(CB_ERR_TIMEOUT, "a bounded device wait ran out (wait sites 0x%x)", word >> 8);
   if (word & cb::kErrBounds) return cb::fail(CB_ERR_BOUNDS, "a slot or block id outside the pool");
   return cb::fail(CB_ERR_INVALID, "device metadata contradicts the host bounds");
 }

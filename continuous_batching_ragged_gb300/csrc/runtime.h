@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "host_common.h"
 
 namespace cb {
@@ -36,5 +38,25 @@ void unlock_aux();
 int sm_count();
 
 cb_status cuda_fail(cudaError_t err, const char* what);
+
+// Launch `kernel` on `stream`.  `after_previous`: programmatic dependent
+// launch -- the grid may start while the kernel launched just before it on
+// the same stream is still running, and must wait for it on the device
+// (griddepcontrol.wait) before reading its results.
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          bool after_previous, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = after_previous ? attr : nullptr;
+  cfg.numAttrs = after_previous ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace cb

@@ -16,7 +16,7 @@ __global__ void bounded_wait_kernel(uint64_t timeout_ns, unsigned* err) {
   __syncthreads();
   // No thread arrives: phase 0 never completes, so the wait must give up.
   const bool ok = cb::sm100::mbar_wait(b, 0, timeout_ns);
-  if (!ok && threadIdx.x == 0) cb::raise_error(err, cb::kErrTimeout);
+  if (!ok && threadIdx.x == 0) cb::raise_error(err, cb::kErrTimeout | cb::kSiteSelfTest);
 }
 
 }  // namespace

@@ -23,6 +23,7 @@
 //   * running max / sum / accumulator per warp, merged across warps in shared
 //     memory, then across splits by the last CTA of the row to finish (an
 //     atomic ticket), which writes the output row.
+#include <algorithm>
 #include <cfloat>
 
 #include "device_common.cuh"
@@ -43,6 +44,11 @@ struct SplitArgs {
   float* partials;          // [rows][H][max_splits][A + 2]
   int32_t* tickets;         // [rows][H]
   int32_t max_splits;
+  const int2* items;        // persistent decode: the plan's (sequence, split) items
+  const int32_t* header;    // persistent decode: [0] = number of items
+  int32_t* claims;          // persistent decode: claim counter
+  int32_t item_cap;         // persistent decode: capacity of the item list
+  uint32_t tag;             // persistent decode: the plan's call tag
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -325,20 +331,30 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs s
   finish_split<T, A, ROW_MODE, EPV, LPR>(sa, pl, split, h, m_run, l_run, acc, sm);
 }
 
-// Decode rows, bf16, head_dim 128, block size a multiple of 16: each warp
-// streams its 16-key K/V tiles (4 KB each, contiguous in the pool) with bulk
-// async copies into a private kStages-deep shared ring, kStages tiles ahead.
-__global__ void __launch_bounds__(kWarps * 32) split_kv_bulk_kernel(const SplitArgs sa) {
+// One decode unit: (sequence, split, head) and the keys [k0, k1) it covers.
+struct Unit {
+  int u;                      // claimed unit index; >= the unit count: no more work
+  int s, t, h, split, nsplit, k0, k1;
+};
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Decode rows, bf16, head_dim 128, block size a multiple of 16, persistent:
+// a fixed grid of CTAs claims units (sequence, split, head) from the step
+// plan until none are left.  Each warp streams its 16-key K/V tiles (4 KB
+// each, contiguous in the pool) with bulk async copies into a private
+// kStages-deep shared ring.  The ring runs across units: once a warp has
+// issued the last tile of its current unit it goes on with the first tiles of
+// the unit the CTA claimed next, so the copies of the next unit are in flight
+// while the current one is merged and written.
+__global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const SplitArgs sa) {
   using T = __nv_bfloat16;
   constexpr int A = 128, EPV = 8, LPR = 16, RPL = 2, NR = 8;
   const AttnArgs& a = sa.a;
-  const int split = blockIdx.x, h = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  RowPlan pl;
-  if (!plan_row<false>(a, split, h, pl)) return;
   const int g = lane / LPR, c = lane % LPR;
-  float qf[EPV];
-  load_q<T, A>(a, pl.t, h, c, qf);
 
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem + warp * kStages * 2 * kTileBytes;                  // [stage][K | V]
@@ -347,70 +363,172 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_bulk_kernel(const SplitA
                warp * kStages;
   MergeSmem<A>& sm = *reinterpret_cast<MergeSmem<A>*>(smem + kWarps * kStages * 2 * kTileBytes +
                                                       kWarps * kStages * 8 + kWarps * kStages * 4);
-  const T* kp = static_cast<const T*>(a.k_pool);
-  const T* vp = static_cast<const T*>(a.v_pool);
-  const int32_t* bt = a.block_tables + size_t(pl.s) * a.max_blocks_per_seq;
-  const int B = a.block_size;
-  const size_t head_off = size_t(h) * B * A;
-  const size_t blk_stride = size_t(a.num_heads) * B * A;
-  const int ntiles = (pl.k1 - pl.k0 + kTile - 1) / kTile;   // tiles of the split; warp takes w, w+4, ...
+  Unit* slots = reinterpret_cast<Unit*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(MergeSmem<A>));   // [2]
+  __shared__ int abort_flag;
   if (lane == 0) {
     for (int st = 0; st < kStages; ++st) sm100::mbar_init(sm100::smem_u32(&bars[st]), 1);
     sm100::fence_mbar_init();
   }
-  __syncwarp();
-  // lane 0: copy the warp's it-th tile into ring slot it % kStages
-  auto issue = [&](int it) {
-    const int j0 = pl.k0 + (warp + kWarps * it) * kTile;
-    const int st = it % kStages;
-    const uint32_t bar = sm100::smem_u32(&bars[st]);
-    const int blk = bt[j0 / B];
-    if (blk >= 0 && blk < a.num_blocks) {
-      valid[st] = 1;
-      const size_t off = size_t(blk) * blk_stride + head_off + size_t(j0 % B) * A;
-      const uint32_t dst = sm100::smem_u32(ring + st * 2 * kTileBytes);
-      sm100::mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-      sm100::bulk_load(dst, kp + off, kTileBytes, bar);
-      sm100::bulk_load(dst + kTileBytes, vp + off, kTileBytes, bar);
-    } else {
-      raise_error(a.err, kErrBounds);
-      valid[st] = 0;
-      sm100::mbar_arrive(bar);
-    }
-  };
-  if (lane == 0)
-    for (int it = 0; it < kStages && warp + kWarps * it < ntiles; ++it) issue(it);
-
-  float m_run = -INFINITY, l_run = 0.f;
-  float acc[EPV];
-#pragma unroll
-  for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
-  for (int it = 0; warp + kWarps * it < ntiles; ++it) {
-    const int st = it % kStages;
-    if (!__all_sync(0xffffffffu, sm100::mbar_wait(sm100::smem_u32(&bars[st]), (it / kStages) & 1))) {
-      if (lane == 0) raise_error(a.err, kErrTimeout);
-      break;
-    }
-    const int base = pl.k0 + (warp + kWarps * it) * kTile;
-    const bool ok = valid[st] != 0;
-    const uint8_t* kt = ring + st * 2 * kTileBytes;
-    uint4 kv[NR], vv[NR];
-#pragma unroll
-    for (int i = 0; i < NR; ++i) {
-      const int r = g + RPL * i;
-      const bool in = ok && base + r < pl.k1;
-      kv[i] = in ? *reinterpret_cast<const uint4*>(kt + r * 256 + c * 16) : make_uint4(0, 0, 0, 0);
-      vv[i] = in ? *reinterpret_cast<const uint4*>(kt + kTileBytes + r * 256 + c * 16) : make_uint4(0, 0, 0, 0);
-    }
-    tile_update<T, EPV, LPR, RPL, NR>(qf, kv, vv, base, pl.k1, lane, m_run, l_run, acc);
-    __syncwarp();                         // every lane has used what it read: the slot may be refilled
-    if (lane == 0 && warp + kWarps * (it + kStages) < ntiles) issue(it + kStages);
+  if (threadIdx.x == 0) abort_flag = 0;
+  grid_dependency_wait();                   // the plan kernel has finished
+  const int H = a.num_heads;
+  const uint32_t seen_tag = uint32_t(__ldcg(sa.header + 4));
+  const int n_items = __ldcg(sa.header);
+  if (seen_tag != sa.tag || n_items < 0 || n_items > sa.item_cap || __ldcg(sa.header + 5) < kSplitKeys) {
+    if (threadIdx.x == 0) raise_error(a.err, kErrInvalid);
+    return;
   }
-  finish_split<T, A, false, EPV, LPR>(sa, pl, split, h, m_run, l_run, acc, sm);
+  const int n_units = n_items * H;
+  const int split_keys = __ldcg(sa.header + 5);            // keys per split, chosen by the plan
+  const T* kp = static_cast<const T*>(a.k_pool);
+  const T* vp = static_cast<const T*>(a.v_pool);
+  const int B = a.block_size;
+  const size_t blk_stride = size_t(H) * B * A;
+
+  // one thread: claim the next unit and describe it in `slot`
+  auto claim = [&](Unit& slot) {
+    Unit U;
+    U.u = abort_flag ? n_units : atomicAdd(sa.claims, 1);
+    if (U.u < n_units) {
+      const int2 it = __ldcg(sa.items + U.u / H);
+      U.h = U.u % H;
+      U.s = it.x;
+      U.split = it.y;
+      bool bad = U.s < 0 || U.s >= a.num_seqs || U.split < 0;
+      int ctx = 0;
+      if (!bad) {
+        U.t = __ldcg(a.cu_seqlens_q + U.s);
+        ctx = __ldcg(a.context_lens + U.s);
+        U.nsplit = (ctx + split_keys - 1) / split_keys;
+        bad = U.t < 0 || U.t >= a.num_tokens || ctx < 1 || ctx > a.max_context_len || U.split >= U.nsplit;
+      }
+      if (bad) {                            // never happens with a plan from this call
+        raise_error(a.err, kErrInvalid);
+        U.u = n_units;
+      } else {
+        U.k0 = U.split * split_keys;
+        U.k1 = min(ctx, U.k0 + split_keys);
+      }
+    }
+    slot = U;
+  };
+  auto load_q_raw = [&](const Unit& U) -> uint4 {
+    return *reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + (size_t(U.t) * H + U.h) * A + c * EPV);
+  };
+  // tiles of unit U that this warp takes (tiles warp, warp + kWarps, ...)
+  auto warp_tiles = [&](const Unit& U) -> int {
+    if (U.u >= n_units) return 0;
+    const int nt = (U.k1 - U.k0 + kTile - 1) / kTile;
+    return nt > warp ? (nt - warp + kWarps - 1) / kWarps : 0;
+  };
+  uint32_t issued = 0, consumed = 0;        // this warp's ring positions (warp-uniform)
+  // lane 0 copies the warp's o-th tile of unit U into the next ring slot
+  auto issue = [&](const Unit& U, int o) {
+    if (lane == 0) {
+      const int j0 = U.k0 + (warp + kWarps * o) * kTile;
+      const int st = issued % kStages;
+      const uint32_t bar = sm100::smem_u32(&bars[st]);
+      const int blk = a.block_tables[size_t(U.s) * a.max_blocks_per_seq + j0 / B];
+      if (blk >= 0 && blk < a.num_blocks) {
+        valid[st] = 1;
+        const size_t off = size_t(blk) * blk_stride + size_t(U.h) * B * A + size_t(j0 % B) * A;
+        const uint32_t dst = sm100::smem_u32(ring + st * 2 * kTileBytes);
+        sm100::mbar_arrive_expect_tx(bar, 2 * kTileBytes);
+        sm100::bulk_load(dst, kp + off, kTileBytes, bar);
+        sm100::bulk_load(dst + kTileBytes, vp + off, kTileBytes, bar);
+      } else {
+        raise_error(a.err, kErrBounds);
+        valid[st] = 0;
+        sm100::mbar_arrive(bar);
+      }
+    }
+    ++issued;
+  };
+
+  // Units are claimed two ahead: unit j lives in slot j % 2.  While unit k
+  // runs, unit k + 1 is known (its first tiles are already being copied) and
+  // one thread claims unit k + 2, so the claim's round trips to L2 hide
+  // behind the tile stream; the claiming thread rotates over the warps.
+  if (threadIdx.x == 0) {
+    claim(slots[0]);
+    claim(slots[1]);
+  }
+  __syncthreads();
+  Unit U0 = slots[0];
+  int n0 = warp_tiles(U0), i0 = 0;          // tiles of U0: count, issued so far
+  uint4 q_raw = make_uint4(0, 0, 0, 0);     // this lane's 16 bytes of U0's query row
+  if (U0.u < n_units) q_raw = load_q_raw(U0);
+  for (int k = 0; U0.u < n_units; ++k) {
+    __syncthreads();                        // slot (k + 1) % 2 written; slot k % 2 read by every thread
+    const Unit U1 = slots[(k + 1) & 1];
+    if (threadIdx.x == (k % kWarps) * 32) claim(slots[k & 1]);
+    const int n1 = warp_tiles(U1);
+    int i1 = 0;
+    auto top_up = [&]() {
+      while (issued - consumed < uint32_t(kStages)) {
+        if (i0 < n0)
+          issue(U0, i0++);
+        else if (i1 < n1)
+          issue(U1, i1++);
+        else
+          break;
+      }
+    };
+    top_up();
+    float qf[EPV];
+    Vec16<T>::to_float(q_raw, qf);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) qf[e] *= a.scale_log2;    // scores in the exp2 domain
+    if (U1.u < n_units) q_raw = load_q_raw(U1);             // in flight while U0 streams
+    float m_run = -INFINITY, l_run = 0.f;
+    float acc[EPV];
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
+    for (int it = 0; it < n0; ++it) {
+      const int st = consumed % kStages;
+      if (!__all_sync(0xffffffffu, sm100::mbar_wait(sm100::smem_u32(&bars[st]), (consumed / kStages) & 1))) {
+        if (lane == 0) {
+          raise_error(a.err, kErrTimeout | kSiteDecodeRing);
+          abort_flag = 1;
+        }
+        break;
+      }
+      const int base = U0.k0 + (warp + kWarps * it) * kTile;
+      const bool ok = valid[st] != 0;
+      const uint8_t* kt = ring + st * 2 * kTileBytes;
+      uint4 kv[NR], vv[NR];
+#pragma unroll
+      for (int i = 0; i < NR; ++i) {
+        const int r = g + RPL * i;
+        const bool in = ok && base + r < U0.k1;
+        kv[i] = in ? *reinterpret_cast<const uint4*>(kt + r * 256 + c * 16) : make_uint4(0, 0, 0, 0);
+        vv[i] = in ? *reinterpret_cast<const uint4*>(kt + kTileBytes + r * 256 + c * 16) : make_uint4(0, 0, 0, 0);
+      }
+      tile_update<T, EPV, LPR, RPL, NR>(qf, kv, vv, base, U0.k1, lane, m_run, l_run, acc);
+      __syncwarp();                         // every lane has used what it read: the slot may be refilled
+      ++consumed;
+      top_up();
+    }
+    RowPlan pl;
+    pl.s = U0.s;
+    pl.t = U0.t;
+    pl.nsplit = U0.nsplit;
+    pl.k0 = U0.k0;
+    pl.k1 = U0.k1;
+    finish_split<T, A, false, EPV, LPR>(sa, pl, U0.split, U0.h, m_run, l_run, acc, sm);
+    U0 = U1;
+    n0 = n1;
+    i0 = i1;
+  }
+  // after a timeout some copies may still be in flight: wait for them (bounded) before exiting
+  while (consumed < issued) {
+    sm100::mbar_wait(sm100::smem_u32(&bars[consumed % kStages]), (consumed / kStages) & 1);
+    ++consumed;
+  }
 }
 
 constexpr uint32_t kBulkSmem = kWarps * kStages * 2 * kTileBytes + kWarps * kStages * (8 + 4) +
-                               sizeof(MergeSmem<128>);
+                               sizeof(MergeSmem<128>) + 2 * sizeof(Unit);
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 bool g_bulk_attr[64] = {};
@@ -419,7 +537,8 @@ bool g_bulk_attr[64] = {};
 
 size_t split_kv_workspace_bytes(bool row_mode, int32_t num_seqs, int32_t num_tokens,
                                 int32_t num_heads, int32_t head_dim, int32_t max_context_len) {
-  const size_t rows = size_t(row_mode ? num_tokens : num_seqs);
+  if (!row_mode) return step_workspace_bytes(num_seqs, num_tokens, num_heads, head_dim, max_context_len);
+  const size_t rows = size_t(num_tokens);
   const size_t splits = size_t((max_context_len + kSplitKeys - 1) / kSplitKeys);
   if (rows == 0 || splits <= 1) return 256;
   return align256(rows * num_heads * sizeof(int32_t)) +
@@ -431,12 +550,86 @@ static void launch(const SplitArgs& sa, dim3 grid, cudaStream_t stream) {
   split_kv_kernel<T, A, ROW><<<grid, kWarps * 32, 0, stream>>>(sa);
 }
 
+int decode_persistent_ctas() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    fail(CB_ERR_UNSUPPORTED, "decode: no usable current device");
+    return 0;
+  }
+  static int ctas_per_sm[64] = {};
+  if (!g_bulk_attr[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(split_kv_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kBulkSmem));
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas_per_sm[dev], split_kv_persistent_kernel,
+                                                        kWarps * 32, kBulkSmem);
+    if (e != cudaSuccess) {
+      cuda_fail(e, "split-KV: kernel attributes");
+      return 0;
+    }
+    if (ctas_per_sm[dev] < 1) ctas_per_sm[dev] = 1;
+    g_bulk_attr[dev] = true;
+  }
+  return ctas_per_sm[dev] * sm_count();
+}
+
+static bool persistent_ok(const AttnArgs& a) {
+  return a.dtype == CB_DTYPE_BF16 && a.head_dim == 128 && a.block_size % kTile == 0;
+}
+
+cb_status launch_decode_persistent(const AttnArgs& a, const StepPlan& plan, bool after_plan,
+                                   cudaStream_t stream) {
+  SplitArgs sa;
+  sa.a = a;
+  sa.tickets = plan.tickets;
+  sa.partials = plan.partials;
+  sa.max_splits = plan.max_splits;
+  sa.items = plan.dec_items;
+  sa.header = plan.header;
+  sa.claims = plan.header + 2;
+  sa.item_cap = plan.dec_cap;
+  sa.tag = plan.tag;
+  if (!persistent_ok(a)) {
+    // other shapes: one CTA per (split, head, sequence); the plan has cleared the tickets
+    if (a.num_seqs > 65535) return fail(CB_ERR_UNSUPPORTED, "split-KV path: more than 65535 rows");
+    const dim3 grid(unsigned(sa.max_splits), unsigned(a.num_heads), unsigned(a.num_seqs));
+    const bool bf16 = a.dtype == CB_DTYPE_BF16;
+    if (bf16 && a.head_dim == 128) launch<__nv_bfloat16, 128, false>(sa, grid, stream);
+    else if (bf16 && a.head_dim == 64) launch<__nv_bfloat16, 64, false>(sa, grid, stream);
+    else if (!bf16 && a.head_dim == 128) launch<float, 128, false>(sa, grid, stream);
+    else if (!bf16 && a.head_dim == 64) launch<float, 64, false>(sa, grid, stream);
+    else return fail(CB_ERR_UNSUPPORTED, "split-KV path: head_dim must be 64 or 128");
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? CB_OK : cuda_fail(e, "split-KV launch");
+  }
+  const int ctas = decode_persistent_ctas();
+  if (ctas < 1) return CB_ERR_CUDA;
+  // never more CTAs than units could exist
+  const int64_t max_units = int64_t(a.num_seqs) * plan.max_splits * a.num_heads;
+  const int64_t grid = std::min<int64_t>(ctas, max_units);
+  if (grid < 1) return CB_OK;
+  cudaError_t e = launch_kernel(split_kv_persistent_kernel, dim3(unsigned(grid)), dim3(kWarps * 32), kBulkSmem,
+                                stream, after_plan, sa);
+  return e == cudaSuccess ? CB_OK : cuda_fail(e, "split-KV: persistent launch");
+}
+
 cb_status launch_split_kv(const AttnArgs& a, bool row_mode, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream) {
   const int32_t rows = row_mode ? a.num_tokens : a.num_seqs;
   if (rows == 0) return CB_OK;
+  if (!row_mode) {
+    // decode rows: step plan, then the decode kernel over its items
+    StepPlan plan;
+    cb_status st = step_plan_layout(workspace, workspace_bytes, a.num_seqs, a.num_tokens, a.num_heads,
+                                    a.head_dim, a.max_context_len, &plan);
+    if (st != CB_OK) return st;
+    plan.dec_ctas = decode_persistent_ctas();
+    st = launch_plan(a, plan, stream);
+    if (st != CB_OK) return st;
+    return launch_decode_persistent(a, plan, true, stream);
+  }
   if (rows > 65535) return fail(CB_ERR_UNSUPPORTED, "split-KV path: more than 65535 rows");
-  SplitArgs sa;
+  SplitArgs sa = {};
   sa.a = a;
   sa.max_splits = (a.max_context_len + kSplitKeys - 1) / kSplitKeys;
   const size_t need = split_kv_workspace_bytes(row_mode, a.num_seqs, a.num_tokens, a.num_heads,
@@ -452,31 +645,13 @@ cb_status launch_split_kv(const AttnArgs& a, bool row_mode, void* workspace,
     cudaError_t e = cudaMemsetAsync(workspace, 0, size_t(rows) * a.num_heads * sizeof(int32_t), stream);
     if (e != cudaSuccess) return cuda_fail(e, "clearing split tickets");
   }
-  dim3 grid(unsigned(sa.max_splits), unsigned(a.num_heads), unsigned(rows));
+  const dim3 grid(unsigned(sa.max_splits), unsigned(a.num_heads), unsigned(rows));
   const bool bf16 = a.dtype == CB_DTYPE_BF16;
-  if (!row_mode && bf16 && a.head_dim == 128 && a.block_size % kTile == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !g_bulk_attr[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(split_kv_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           int(kBulkSmem));
-      if (e != cudaSuccess) return cuda_fail(e, "split-KV: shared memory attribute");
-      g_bulk_attr[dev] = true;
-    }
-    split_kv_bulk_kernel<<<grid, kWarps * 32, kBulkSmem, stream>>>(sa);
-  } else if (bf16 && a.head_dim == 128) {
-    row_mode ? launch<__nv_bfloat16, 128, true>(sa, grid, stream)
-             : launch<__nv_bfloat16, 128, false>(sa, grid, stream);
-  } else if (bf16 && a.head_dim == 64) {
-    row_mode ? launch<__nv_bfloat16, 64, true>(sa, grid, stream)
-             : launch<__nv_bfloat16, 64, false>(sa, grid, stream);
-  } else if (!bf16 && a.head_dim == 128) {
-    row_mode ? launch<float, 128, true>(sa, grid, stream) : launch<float, 128, false>(sa, grid, stream);
-  } else if (!bf16 && a.head_dim == 64) {
-    row_mode ? launch<float, 64, true>(sa, grid, stream) : launch<float, 64, false>(sa, grid, stream);
-  } else {
-    return fail(CB_ERR_UNSUPPORTED, "split-KV path: head_dim must be 64 or 128");
-  }
+  if (bf16 && a.head_dim == 128) launch<__nv_bfloat16, 128, true>(sa, grid, stream);
+  else if (bf16 && a.head_dim == 64) launch<__nv_bfloat16, 64, true>(sa, grid, stream);
+  else if (!bf16 && a.head_dim == 128) launch<float, 128, true>(sa, grid, stream);
+  else if (!bf16 && a.head_dim == 64) launch<float, 64, true>(sa, grid, stream);
+  else return fail(CB_ERR_UNSUPPORTED, "split-KV path: head_dim must be 64 or 128");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "split-KV launch");
   return CB_OK;
