@@ -250,6 +250,73 @@ def time_oracle(b, budget_s: float):
 # serving trace: the scheduler drives every step
 # ---------------------------------------------------------------------------
 
+def run_trace_graph(torch, api, W, requests, *, num_layers, num_heads, head_dim, block_size,
+                    token_budget, num_blocks, seed, max_steps=100000):
+    """run_trace with each step captured once as a CUDA graph (StepGraph):
+    per step the host builds the batch, the device generator writes every
+    layer's Q/K/V (not timed), the metadata is copied into the graph's fixed
+    buffers, and the timed region is one graph replay -- the step plan, then
+    cb_append_kv_dims + cb_ragged_attention_planned for every layer."""
+    from continuous_batching_ragged_gb300.step_graph import StepGraph
+    dt = torch.bfloat16
+    caches = [api.KVCache.empty(num_blocks, num_heads, block_size, head_dim, dt) for _ in range(num_layers)]
+    for c in caches:
+        c.k.zero_()
+        c.v.zero_()
+    longest = max(r.prompt_len + r.output_len for r in requests)
+    max_blocks = (longest + block_size - 1) // block_size + 1
+    shape = (token_budget, num_heads, head_dim)
+    q, k, v = ([torch.zeros(shape, dtype=dt, device="cuda") for _ in range(num_layers)] for _ in range(3))
+    out = [torch.zeros(shape, dtype=dt, device="cuda")]
+    sg = StepGraph(caches, q, k, v, out, max_seqs=token_budget, max_blocks_per_seq=max_blocks,
+                   scale=1.0 / math.sqrt(head_dim))
+    sched = api.Scheduler(token_budget, block_size, num_blocks)
+    for r in requests:
+        sched.add_request(r.id, r.arrival_step, r.prompt_len, r.output_len)
+    steps = []
+    stream = torch.cuda.current_stream()
+    for step in range(max_steps):
+        t0 = time.perf_counter()
+        bt = sched.build_batch()
+        t_sched = time.perf_counter() - t0
+        S, T = bt.num_seqs, bt.T
+        if S == 0:
+            t0 = time.perf_counter()
+            sched.complete_step()
+            t_sched += time.perf_counter() - t0
+            if sched.idle:
+                break
+            steps.append({"T": 0, "sched_s": t_sched, "gpu_ms": 0.0})
+            continue
+        rows = torch.from_numpy(np.repeat(bt.request_ids, bt.q_lens).astype(np.int64)).cuda()
+        pos = torch.from_numpy(np.concatenate([np.arange(c - n, c) for c, n in
+                                               zip(bt.context_lens, bt.q_lens)]).astype(np.int32)).cuda()
+        for layer in range(num_layers):
+            for kind, t in ((W.KIND_Q, q[layer]), (W.KIND_K, k[layer]), (W.KIND_V, v[layer])):
+                api.cb_synth_tokens(t[:T], seed, kind, layer, rows, pos)
+        sg.load(bt.cu_seqlens_q, bt.context_lens, bt.block_tables, bt.slot_mapping, bt.max_q_len,
+                bt.max_context_len)
+        if sg.graph is None:
+            sg.run_eager()                 # resolves per-device state; the replay below redoes the step
+            torch.cuda.synchronize()
+            sg.capture()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        sg.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        api.cb_check_device_errors()
+        t0 = time.perf_counter()
+        sched.complete_step()
+        t_sched += time.perf_counter() - t0
+        steps.append({"T": T, "S": S, "decode": bt.num_decode, "sched_s": t_sched,
+                      "gpu_ms": e0.elapsed_time(e1), "kv_tokens": int(np.sum(bt.context_lens)),
+                      "q_lens": bt.q_lens, "max_q_len": bt.max_q_len, "ctx": bt.context_lens})
+    del sg, caches
+    torch.cuda.empty_cache()
+    return steps
+
+
 def run_trace(torch, api, W, requests, *, num_layers, num_heads, head_dim, block_size,
               token_budget, num_blocks, seed, on_layer=None, max_steps=100000):
     """Serve ``requests`` to completion.  Each step: cb_build_batch on the host,
@@ -413,8 +480,9 @@ def run_reference(args, b, label):
     print(json.dumps(line), flush=True)
 
 
-def run_trace_bench(args):
-    """The serving trace end to end: 2000 requests, 32 layers, budget 4096."""
+def run_trace_bench(args, graph=False):
+    """The serving trace end to end: 2000 requests, 32 layers, budget 4096
+    (graph: each step one CUDA-graph replay)."""
     from continuous_batching_ragged_gb300 import workloads as W
     cfg = W.SERVING_TRACE
     reqs = W.serving_trace()
@@ -449,12 +517,13 @@ def run_trace_bench(args):
     kw = dict(num_layers=cfg["num_layers"], num_heads=cfg["num_heads"], head_dim=cfg["head_dim"],
               block_size=cfg["block_size"], token_budget=cfg["token_budget"],
               num_blocks=cfg["num_blocks"], seed=4)
+    runner = run_trace_graph if graph else run_trace
     # warm-up: a short trace of the first requests
-    run_trace(torch, api, W, reqs[:16], max_steps=max(3, args.warmup), **kw)
+    runner(torch, api, W, reqs[:16], max_steps=max(3, args.warmup), **kw)
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     t0 = time.perf_counter()
-    steps = run_trace(torch, api, W, reqs, **kw)
+    steps = runner(torch, api, W, reqs, **kw)
     wall = time.perf_counter() - t0
     clocks = sampler.stop()
     busy = [st for st in steps if st["T"] > 0]
@@ -479,7 +548,13 @@ def run_trace_bench(args):
                               "bytes_total": sum(r[1] for r in roof), "flops_total": sum(r[2] for r in roof)},
             "scheduler_us_per_step": sched_us, "wall_s": wall,
             "mean_decode_per_step": float(np.mean([st["decode"] for st in busy])),
-            "clocks": clocks, "gpu_launches": sum(cfg["num_layers"] * launches_per_layer(st) for st in busy)}
+            "clocks": clocks,
+            "gpu_launches": (sum(1 + 3 * cfg["num_layers"] for st in busy) if graph else
+                             sum(cfg["num_layers"] * launches_per_layer(st) for st in busy))}
+    if graph:
+        line["config"]["workload"] = label + "_graph"
+        line["config"]["timed"] = ("one CUDA-graph replay per step: the step plan, then cb_append_kv_dims + "
+                                   "cb_ragged_attention_planned of every layer; Q/K/V generation not timed")
     print(json.dumps(line), flush=True)
 
 
@@ -489,7 +564,8 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "mixed", "long", "tiny", "trace", "mixed_padded", "insertion", "insertion_padded"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "mixed", "long", "tiny", "trace", "trace_graph",
+                                                             "mixed_padded", "insertion", "insertion_padded"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-seqs", type=int, default=256,
@@ -498,8 +574,8 @@ def main():
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 
-    if args.workload == "trace":
-        run_trace_bench(args)
+    if args.workload in ("trace", "trace_graph"):
+        run_trace_bench(args, graph=args.workload == "trace_graph")
         return
     b, label = make_workload(args.workload, args.decode_seqs)
     if args.impl == "reference":
@@ -599,7 +675,7 @@ def main():
     t_dec = work["decode_bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_pre = work["prefill_flops"] / (peaks["bf16_tflops"] * 1e12)
     if t_dec >= t_pre:
-        dom = {"kernel": "split_kv_bulk_kernel (decode rows)" if b.dtype == "bf16" else "split_kv_kernel",
+        dom = {"kernel": "split_kv_persistent_kernel (decode rows)" if b.dtype == "bf16" else "split_kv_kernel",
                "bound": "hbm", "achieved": work["decode_bytes"] / (attn_ms * 1e-3) / 1e9,
                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
@@ -608,9 +684,9 @@ def main():
                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     dom["frac"] = dom["achieved"] / dom["peak"]
     if dom["bound"] == "hbm":
-        prof, alg = "split_kv_bulk_decode_64seq.md", work["decode_bytes"]
+        prof, alg = "split_kv_persistent_decode_64seq.md", work["decode_bytes"]
     else:
-        prof, alg = "prefill_tc_long_prompt_last_chunk.md", work["prefill_bytes"]
+        prof, alg = "prefill_tc_persistent_long_prompt_last_chunk.md", work["prefill_bytes"]
     ratio = profiled_traffic_ratio(prof) if b.dtype == "bf16" else None
     dom["traffic"] = None if ratio is None else ratio * alg
     if ratio is not None:

@@ -110,6 +110,46 @@ def cb_ragged_attention(q: torch.Tensor, cache: KVCache, cu_seqlens_q: torch.Ten
     return out
 
 
+def cb_append_kv_dims(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                      dims: torch.Tensor, cache: KVCache, stream=None) -> None:
+    """cb_append_kv with the token count in dims[1] (device); k_new's rows bound it."""
+    if slot_mapping.dtype != torch.int64 or dims.dtype != torch.int32:
+        raise ValueError("slot_mapping must be int64 and dims int32")
+    c = cache.c_struct()
+    check(native.lib().cb_append_kv_dims(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(dims),
+                                         k_new.shape[0], ctypes.byref(c), _stream_handle(stream)),
+          "cb_append_kv_dims")
+
+
+def cb_plan_step(cache: KVCache, cu_seqlens_q: torch.Tensor, context_lens: torch.Tensor, *,
+                 num_tokens: int, max_blocks_per_seq: int, max_q_len: int, max_context_len: int,
+                 workspace: torch.Tensor, dims: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Build the step's work lists in `workspace` (sizes are capacities when dims is given)."""
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("context_lens", context_lens)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    c = cache.c_struct()
+    check(native.lib().cb_plan_step(
+        ctypes.byref(c), _ptr(cu_seqlens_q), _ptr(context_lens), _ptr(dims), context_lens.shape[0],
+        num_tokens, max_blocks_per_seq, max_q_len, max_context_len, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream)), "cb_plan_step")
+
+
+def cb_ragged_attention_planned(q: torch.Tensor, cache: KVCache, cu_seqlens_q: torch.Tensor,
+                                context_lens: torch.Tensor, block_tables: torch.Tensor, *,
+                                max_q_len: int, max_context_len: int, scale: float, out: torch.Tensor,
+                                workspace: torch.Tensor, dims: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    """cb_ragged_attention over the plan cb_plan_step built in `workspace`."""
+    c = cache.c_struct()
+    check(native.lib().cb_ragged_attention_planned(
+        _ptr(q), ctypes.byref(c), _ptr(cu_seqlens_q), _ptr(context_lens), _ptr(block_tables), _ptr(dims),
+        context_lens.shape[0], q.shape[0], block_tables.shape[1], max_q_len, max_context_len, float(scale),
+        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream)),
+        "cb_ragged_attention_planned")
+    return out
+
+
 def cb_decode_attention_noalloc(q: torch.Tensor, cache: KVCache, cu_seqlens_q: torch.Tensor,
                                 context_lens: torch.Tensor, block_tables: torch.Tensor, *,
                                 max_context_len: int, scale: float, out: torch.Tensor,

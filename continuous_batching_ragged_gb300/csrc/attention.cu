@@ -13,6 +13,8 @@
 // its list first leaves its SMs to the other.  fp32 caches take the CUDA-core
 // kernel for every row.
 #include <cmath>
+#include <mutex>
+#include <unordered_map>
 
 #include "kernels.h"
 #include "runtime.h"
@@ -49,38 +51,38 @@ extern "C" size_t cb_attention_workspace_size(const cb_kv_cache* cache, int32_t 
                                       cache->head_dim, max_context_len);
 }
 
-extern "C" cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache,
-                                         const int32_t* cu_seqlens_q, const int32_t* context_lens,
-                                         const int32_t* block_tables, int32_t num_seqs,
-                                         int32_t num_tokens, int32_t max_blocks_per_seq,
-                                         int32_t max_q_len, int32_t max_context_len, float scale,
-                                         void* out, void* workspace, size_t workspace_bytes,
-                                         void* stream) {
-  const char* who = "cb_ragged_attention";
+namespace {
+
+// Host-side checks shared by every attention entry point; fills `a`.
+cb_status prepare(const char* who, const void* q, const cb_kv_cache* cache, const int32_t* cu_seqlens_q,
+                  const int32_t* context_lens, const int32_t* block_tables, int32_t num_seqs, int32_t num_tokens,
+                  int32_t max_blocks_per_seq, int32_t max_q_len, int32_t max_context_len, float scale, void* out,
+                  const int32_t* dims, bool plan_only, cb::AttnArgs& a) {
   cb_status st = check_cache(cache, who);
   if (st != CB_OK) return st;
   if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq < 0 || max_q_len < 0 || max_context_len < 0)
     return cb::fail(CB_ERR_INVALID, "%s: negative size", who);
   if (num_seqs == 0 || num_tokens == 0) {
-    if (num_seqs != num_tokens && (num_seqs == 0) != (num_tokens == 0))
+    if ((num_seqs == 0) != (num_tokens == 0))
       return cb::fail(CB_ERR_INVALID, "%s: num_seqs and num_tokens must both be zero or both positive", who);
     return CB_OK;
   }
-  if (num_tokens < num_seqs) return cb::fail(CB_ERR_INVALID, "%s: fewer tokens than sequences", who);
+  if (!dims && num_tokens < num_seqs) return cb::fail(CB_ERR_INVALID, "%s: fewer tokens than sequences", who);
   if (max_q_len < 1 || max_q_len > num_tokens || max_context_len < max_q_len)
     return cb::fail(CB_ERR_INVALID, "%s: need 1 <= max_q_len <= num_tokens and max_q_len <= max_context_len", who);
   if (int64_t(max_blocks_per_seq) * cache->block_size < max_context_len)
     return cb::fail(CB_ERR_INVALID, "%s: max_blocks_per_seq * block_size < max_context_len", who);
-  if (!(scale > 0.f) || !std::isfinite(scale)) return cb::fail(CB_ERR_INVALID, "%s: scale must be finite and > 0", who);
-  if (!q || !cu_seqlens_q || !context_lens || !block_tables || !out || !cache->k || !cache->v)
-    return cb::fail(CB_ERR_INVALID, "%s: null pointer", who);
-  const uintptr_t align = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
-                          reinterpret_cast<uintptr_t>(cache->k) | reinterpret_cast<uintptr_t>(cache->v);
-  if (align % 16 != 0) return cb::fail(CB_ERR_INVALID, "%s: q, out and the pools must be 16-byte aligned", who);
-
+  if (!cu_seqlens_q || !context_lens) return cb::fail(CB_ERR_INVALID, "%s: null pointer", who);
+  if (!plan_only) {
+    if (!(scale > 0.f) || !std::isfinite(scale))
+      return cb::fail(CB_ERR_INVALID, "%s: scale must be finite and > 0", who);
+    if (!q || !block_tables || !out || !cache->k || !cache->v) return cb::fail(CB_ERR_INVALID, "%s: null pointer", who);
+    const uintptr_t align = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
+                            reinterpret_cast<uintptr_t>(cache->k) | reinterpret_cast<uintptr_t>(cache->v);
+    if (align % 16 != 0) return cb::fail(CB_ERR_INVALID, "%s: q, out and the pools must be 16-byte aligned", who);
+  }
   unsigned* err = cb::device_error_word();
   if (!err) return CB_ERR_CUDA;
-  cb::AttnArgs a;
   a.q = q;
   a.out = out;
   a.k_pool = cache->k;
@@ -100,22 +102,12 @@ extern "C" cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache
   a.scale_log2 = scale * 1.4426950408889634f;
   a.dtype = cache->dtype;
   a.err = err;
-  cudaStream_t main = static_cast<cudaStream_t>(stream);
+  a.dims = dims;
+  return CB_OK;
+}
 
-  if (cache->dtype == CB_DTYPE_F32) return cb::launch_split_kv(a, true, workspace, workspace_bytes, main);
-
-  // bf16: the step plan first, then the persistent kernels over its work lists
-  cb::StepPlan plan;
-  st = cb::step_plan_layout(workspace, workspace_bytes, num_seqs, num_tokens, cache->num_heads,
-                            cache->head_dim, max_context_len, &plan);
-  if (st != CB_OK) return st;
-  plan.dec_ctas = cb::decode_persistent_ctas();
-  st = cb::launch_plan(a, plan, main);
-  if (st != CB_OK) return st;
-  if (max_q_len == 1) return cb::launch_decode_persistent(a, plan, true, main);
-  if (max_q_len == num_tokens && num_seqs == 1) return cb::launch_prefill_tc(a, plan, true, main);
-
-  // Mixed step: prefill chunks on the auxiliary stream, decode rows on `stream`.
+// Prefill chunks on the auxiliary stream, decode rows on `main`, joined.
+cb_status run_both(const cb::AttnArgs& a, const cb::StepPlan& plan, cudaStream_t main) {
   cb::AuxStream* aux = cb::aux_stream();
   if (!aux) return CB_ERR_CUDA;
   cb::lock_aux();
@@ -132,4 +124,119 @@ extern "C" cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache
   cb::unlock_aux();
   if (e != cudaSuccess) return cb::cuda_fail(e, "joining the auxiliary stream");
   return sp != CB_OK ? sp : sd;
+}
+
+// Plans built by cb_plan_step, by workspace: what the planned attention calls
+// must match.
+struct PlanRecord {
+  cb::StepPlan plan;
+  const int32_t *cu, *ctx, *dims;
+  int32_t num_seqs, num_tokens, max_blocks_per_seq, max_q_len, max_context_len;
+  int32_t num_heads, head_dim, block_size, num_blocks;
+  size_t workspace_bytes;
+};
+std::mutex g_plans_mutex;
+std::unordered_map<const void*, PlanRecord> g_plans;
+
+}  // namespace
+
+extern "C" cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache,
+                                         const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                         const int32_t* block_tables, int32_t num_seqs,
+                                         int32_t num_tokens, int32_t max_blocks_per_seq,
+                                         int32_t max_q_len, int32_t max_context_len, float scale,
+                                         void* out, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+  cb::AttnArgs a;
+  cb_status st = prepare("cb_ragged_attention", q, cache, cu_seqlens_q, context_lens, block_tables, num_seqs,
+                         num_tokens, max_blocks_per_seq, max_q_len, max_context_len, scale, out, nullptr, false,
+                         a);
+  if (st != CB_OK || num_seqs == 0) return st;
+  cudaStream_t main = static_cast<cudaStream_t>(stream);
+  if (cache->dtype == CB_DTYPE_F32) return cb::launch_split_kv(a, true, workspace, workspace_bytes, main);
+
+  // bf16: the step plan first, then the persistent kernels over its work lists
+  cb::StepPlan plan;
+  st = cb::step_plan_layout(workspace, workspace_bytes, num_seqs, num_tokens, cache->num_heads,
+                            cache->head_dim, max_context_len, &plan);
+  if (st != CB_OK) return st;
+  plan.dec_ctas = cb::decode_persistent_ctas();
+  st = cb::launch_plan(a, plan, main);
+  if (st != CB_OK) return st;
+  if (max_q_len == 1) return cb::launch_decode_persistent(a, plan, true, main);
+  if (max_q_len == num_tokens && num_seqs == 1) return cb::launch_prefill_tc(a, plan, true, main);
+  return run_both(a, plan, main);
+}
+
+extern "C" cb_status cb_plan_step(const cb_kv_cache* cache, const int32_t* cu_seqlens_q,
+                                  const int32_t* context_lens, const int32_t* dims, int32_t num_seqs,
+                                  int32_t num_tokens, int32_t max_blocks_per_seq, int32_t max_q_len,
+                                  int32_t max_context_len, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  const char* who = "cb_plan_step";
+  if (!cache) return cb::fail(CB_ERR_INVALID, "%s: null cache", who);
+  if (cache->dtype != CB_DTYPE_BF16 || cache->block_size % 16 != 0)
+    return cb::fail(CB_ERR_UNSUPPORTED, "%s: planned steps need bf16 and a block size multiple of 16", who);
+  // the plan reads only the metadata (q, out, block tables and pools are not needed)
+  cb::AttnArgs a;
+  cb_status st = prepare(who, nullptr, cache, cu_seqlens_q, context_lens, nullptr, num_seqs, num_tokens,
+                         max_blocks_per_seq, max_q_len, max_context_len, 1.0f, nullptr, dims, true, a);
+  if (st != CB_OK) return st;
+  if (num_seqs == 0) return CB_OK;
+  PlanRecord rec;
+  st = cb::step_plan_layout(workspace, workspace_bytes, num_seqs, num_tokens, cache->num_heads, cache->head_dim,
+                            max_context_len, &rec.plan);
+  if (st != CB_OK) return st;
+  rec.plan.dec_ctas = cb::decode_persistent_ctas();
+  st = cb::launch_plan(a, rec.plan, static_cast<cudaStream_t>(stream));
+  if (st != CB_OK) return st;
+  rec.cu = cu_seqlens_q;
+  rec.ctx = context_lens;
+  rec.dims = dims;
+  rec.num_seqs = num_seqs;
+  rec.num_tokens = num_tokens;
+  rec.max_blocks_per_seq = max_blocks_per_seq;
+  rec.max_q_len = max_q_len;
+  rec.max_context_len = max_context_len;
+  rec.num_heads = cache->num_heads;
+  rec.head_dim = cache->head_dim;
+  rec.block_size = cache->block_size;
+  rec.num_blocks = cache->num_blocks;
+  rec.workspace_bytes = workspace_bytes;
+  std::lock_guard<std::mutex> lock(g_plans_mutex);
+  g_plans[workspace] = rec;
+  return CB_OK;
+}
+
+extern "C" cb_status cb_ragged_attention_planned(const void* q, const cb_kv_cache* cache,
+                                                 const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                                 const int32_t* block_tables, const int32_t* dims,
+                                                 int32_t num_seqs, int32_t num_tokens,
+                                                 int32_t max_blocks_per_seq, int32_t max_q_len,
+                                                 int32_t max_context_len, float scale, void* out,
+                                                 void* workspace, size_t workspace_bytes, void* stream) {
+  const char* who = "cb_ragged_attention_planned";
+  cb::AttnArgs a;
+  cb_status st = prepare(who, q, cache, cu_seqlens_q, context_lens, block_tables, num_seqs, num_tokens,
+                         max_blocks_per_seq, max_q_len, max_context_len, scale, out, dims, false, a);
+  if (st != CB_OK || num_seqs == 0) return st;
+  PlanRecord rec;
+  {
+    std::lock_guard<std::mutex> lock(g_plans_mutex);
+    auto it = g_plans.find(workspace);
+    if (it == g_plans.end()) return cb::fail(CB_ERR_INVALID, "%s: no cb_plan_step was made in this workspace", who);
+    rec = it->second;
+  }
+  if (rec.cu != cu_seqlens_q || rec.ctx != context_lens || rec.dims != dims || rec.num_seqs != num_seqs ||
+      rec.num_tokens != num_tokens || rec.max_blocks_per_seq != max_blocks_per_seq || rec.max_q_len != max_q_len ||
+      rec.max_context_len != max_context_len || rec.num_heads != cache->num_heads ||
+      rec.head_dim != cache->head_dim || rec.block_size != cache->block_size ||
+      rec.num_blocks != cache->num_blocks || rec.workspace_bytes != workspace_bytes)
+    return cb::fail(CB_ERR_INVALID, "%s: the workspace's plan was made for other metadata, sizes or cache shape",
+                    who);
+  cudaStream_t main = static_cast<cudaStream_t>(stream);
+  // the claim counters start at zero for every call over the plan
+  cudaError_t e = cudaMemsetAsync(rec.plan.header + 2, 0, 2 * sizeof(int32_t), main);
+  if (e != cudaSuccess) return cb::cuda_fail(e, "clearing the claim counters");
+  return run_both(a, rec.plan, main);
 }

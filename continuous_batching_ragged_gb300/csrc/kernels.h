@@ -29,6 +29,10 @@ struct AttnArgs {
   float scale_log2;       // softmax scale * log2(e)
   cb_dtype dtype;
   unsigned* err;
+  // Device step sizes (num_seqs, num_tokens, max_q_len, max_context_len), or
+  // null.  When set, the four host sizes above are capacities: buffer extents
+  // that bound the device values, which only the step plan reads.
+  const int32_t* dims = nullptr;
 };
 
 // Keys per split of the register split-KV kernel, and the smallest split of
@@ -36,7 +40,7 @@ struct AttnArgs {
 // step and stores in header[5]).  Workspaces are sized for this split.
 constexpr int kSplitKeys = 512;
 
-// Query rows per work item of the prefill kernel (two 128-row tiles).
+// Query rows per prefill unit (two 128-row tiles).
 constexpr int kPrefillPairRows = 256;
 
 // The step's work lists, built on the GPU from the packed metadata by
@@ -44,17 +48,19 @@ constexpr int kPrefillPairRows = 256;
 // claim items through the counters in `header`.  All pointers are into the
 // caller's workspace.
 struct StepPlan {
-  int32_t* header;        // [0] decode items, [1] prefill items, [2] decode claims, [3] prefill claims,
-                          // [4] call tag, [5] keys per decode split
+  int32_t* header;        // [0] decode items, [1] prefill units, [2] decode claims, [3] prefill claims,
+                          // [4] call tag, [5] keys per decode split, [6] num_seqs, [7] num_tokens
   int2* dec_items;        // (sequence, split) of every q_len == 1 row, longest first
   int2* dec_scratch;      // the decode items before sorting
-  int2* pre_items;        // (sequence, 256-row query pair) of every q_len > 1 chunk, costliest first
-  int2* pre_scratch;      // the prefill items before sorting
+  int2* pre_seqs;         // (sequence, query pairs) of every q_len > 1 chunk, costliest chunk first
+  int2* pre_scratch;      // the same records before sorting
+  int2* pre_units;        // prefill units (sequence, pair | head << 16): chunk by chunk in
+                          // pre_seqs order, head-major within a chunk, costliest pair first
   int32_t* tickets;       // [num_seqs][H] split arrival counters, zeroed by the plan
   float* partials;        // [num_seqs][H][max_splits][A + 2] split results (acc, max, sum)
   int32_t max_splits;
   int32_t dec_cap;        // capacity of dec_items
-  int32_t pre_cap;        // capacity of pre_items and pre_scratch
+  int32_t pre_cap;        // capacity of pre_seqs and pre_scratch (pre_units holds pre_cap * H)
   uint32_t tag;           // this call's tag: the plan writes it to header[4], the kernels check it
   int32_t dec_ctas;       // CTAs of the persistent decode grid (sets the split length)
 };

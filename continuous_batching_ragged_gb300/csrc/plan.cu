@@ -9,12 +9,14 @@
 // that does not exist (a split past a short context, a prefill tile of a
 // decode row), and the launch shape no longer depends on the batch, which is
 // what lets a whole step be captured once in a CUDA graph.
-//   * decode items: (sequence, split) for every q_len == 1 row, one per 512
-//     keys of its context, in sequence order;
-//   * prefill items: (sequence, pair of 128-row query tiles) for every
-//     q_len > 1 chunk, sorted by cost (KV tiles x query tiles, descending) so
-//     that greedy claiming is longest-first.
-// Each list item stands for num_heads units, one per head.
+//   * decode items: (sequence, split) for every q_len == 1 row, one per
+//     split of its context, sorted by length (longest first, so that greedy
+//     claiming ends on short units); the split length is chosen per step;
+//   * prefill units: (sequence, pair of 128-row query tiles, head) for every
+//     q_len > 1 chunk; chunks by total cost (KV tiles x query tiles,
+//     costliest first), then head by head, so the pairs of one (sequence,
+//     head) share its K/V tiles in L2.
+// A decode item stands for num_heads units, one per head.
 #include <atomic>
 
 #include "device_common.cuh"
@@ -27,6 +29,7 @@ namespace {
 constexpr int kPlanThreads = 1024;
 constexpr int kCostBuckets = 4096;     // costs at or above the last bucket share it
 constexpr int kUnitsPerCta = 6;        // decode units per persistent CTA the split size aims for
+constexpr int kRowCache = 2048;        // rows whose (q_len, ctx) stay in shared memory after pass 1
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -79,14 +82,20 @@ struct RowInfo {
   bool bad;
 };
 
-__device__ __forceinline__ RowInfo row_info(const AttnArgs& a, int s) {
+// The step's sizes: the host's, or (when AttnArgs::dims is set) the device's,
+// checked against the host capacities.
+struct StepSizes {
+  int num_seqs, num_tokens, max_q_len, max_context_len;
+};
+
+__device__ __forceinline__ RowInfo row_info(const AttnArgs& a, const StepSizes& z, int s) {
   RowInfo r;
   const int c0 = a.cu_seqlens_q[s];
   const int c1 = a.cu_seqlens_q[s + 1];
   r.q_len = c1 - c0;
   r.ctx = a.context_lens[s];
-  r.bad = r.q_len < 1 || r.ctx < r.q_len || r.ctx > a.max_context_len || r.q_len > a.max_q_len || c0 < 0 ||
-          c1 > a.num_tokens || (int64_t(r.ctx) + a.block_size - 1) / a.block_size > a.max_blocks_per_seq;
+  r.bad = r.q_len < 1 || r.ctx < r.q_len || r.ctx > z.max_context_len || r.q_len > z.max_q_len || c0 < 0 ||
+          c1 > z.num_tokens || (int64_t(r.ctx) + a.block_size - 1) / a.block_size > a.max_blocks_per_seq;
   return r;
 }
 
@@ -129,12 +138,30 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
   launch_dependents();                      // they wait for this grid on the device
   __shared__ uint64_t warp_sums[32];
   __shared__ uint32_t bucket[kCostBuckets];
+  __shared__ int2 row_cache[kRowCache];     // (q_len, or 0 for a bad row; ctx)
   const int tid = threadIdx.x;
+  StepSizes z = {a.num_seqs, a.num_tokens, a.max_q_len, a.max_context_len};
+  if (a.dims) {
+    z = StepSizes{a.dims[0], a.dims[1], a.dims[2], a.dims[3]};
+    if (z.num_seqs < 0 || z.num_seqs > a.num_seqs || z.num_tokens < 0 || z.num_tokens > a.num_tokens ||
+        z.max_q_len < 0 || z.max_q_len > a.max_q_len || z.max_context_len < 0 ||
+        z.max_context_len > a.max_context_len) {
+      if (tid == 0) raise_error(a.err, kErrInvalid);   // sizes beyond the capacities: an empty step
+      z.num_seqs = 0;
+    }
+  }
+  // (q_len, ctx) of row s after pass 1; q_len 0 marks a row left out
+  auto row = [&](int s) -> int2 {
+    if (s < kRowCache) return row_cache[s];
+    const RowInfo r = row_info(a, z, s);
+    return make_int2(r.bad ? 0 : r.q_len, r.ctx);
+  };
 
   // Pass 1: check every row; total keys of the decode rows.
   uint64_t dec_keys = 0;
-  for (int s = tid; s < a.num_seqs; s += kPlanThreads) {
-    const RowInfo r = row_info(a, s);
+  for (int s = tid; s < z.num_seqs; s += kPlanThreads) {
+    const RowInfo r = row_info(a, z, s);
+    if (s < kRowCache) row_cache[s] = make_int2(r.bad ? 0 : r.q_len, r.ctx);
     if (r.bad)
       raise_error(a.err, kErrInvalid);
     else if (r.q_len == 1)
@@ -153,16 +180,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
 
   // Pass 2: list the items (unsorted).
   uint64_t base = 0;                        // items so far: decode in the low, prefill in the high word
-  for (int s0 = 0; s0 < a.num_seqs; s0 += kPlanThreads) {
+  for (int s0 = 0; s0 < z.num_seqs; s0 += kPlanThreads) {
     const int s = s0 + tid;
-    uint32_t nd = 0, np = 0;
-    if (s < a.num_seqs) {
-      const RowInfo r = row_info(a, s);
-      if (!r.bad) {
-        if (r.q_len == 1)
-          nd = uint32_t((r.ctx + split - 1) / split);
-        else
-          np = uint32_t((r.q_len + kPrefillPairRows - 1) / kPrefillPairRows);
+    uint32_t nd = 0, np = 0, pairs = 0;     // decode items; prefill records (0 or 1) and their pairs
+    if (s < z.num_seqs) {
+      const int2 r = row(s);
+      if (r.x > 0) {
+        if (r.x == 1) {
+          nd = uint32_t((r.y + split - 1) / split);
+        } else {
+          np = 1;
+          pairs = uint32_t((r.x + kPrefillPairRows - 1) / kPrefillPairRows);
+        }
       }
     }
     uint64_t total;
@@ -177,39 +206,65 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
       }
     }
     if (np > 0) {
-      if (op + np <= uint32_t(p.pre_cap)) {
-        for (uint32_t k = 0; k < np; ++k) p.pre_scratch[op + k] = make_int2(s, int(k));
-      } else {
+      if (op < uint32_t(p.pre_cap))
+        p.pre_scratch[op] = make_int2(s, int(pairs));
+      else
         raise_error(a.err, kErrInvalid);      // overlapping query ranges (malformed cu_seqlens_q)
-      }
     }
   }
   const int n_dec = min(int(uint32_t(base)), p.dec_cap);
-  const int n_pre = min(int(uint32_t(base >> 32)), p.pre_cap);
+  const int n_chunks = min(int(uint32_t(base >> 32)), p.pre_cap);
   // split tickets start at zero (coalesced over the whole [num_seqs][H] array)
-  for (int i = tid; i < a.num_seqs * a.num_heads; i += kPlanThreads) p.tickets[i] = 0;
+  for (int i = tid; i < z.num_seqs * a.num_heads; i += kPlanThreads) p.tickets[i] = 0;
   __syncthreads();                          // every thread's items are written before any is re-read
 
   // Longest first, so that greedy claiming ends on short units.
   sort_desc(p.dec_scratch, p.dec_items, n_dec,
             [&](int2 it) {
-              const int len = min(a.context_lens[it.x] - it.y * split, split);
+              const int len = min(row(it.x).y - it.y * split, split);
               return (len + 15) / 16;
             },
             bucket, warp_sums);
-  sort_desc(p.pre_scratch, p.pre_items, n_pre,
-            [&](int2 it) {
-              const int q_len = a.cu_seqlens_q[it.x + 1] - a.cu_seqlens_q[it.x];
-              return pair_cost(q_len, a.context_lens[it.x], it.y);
+  // Prefill: chunks by total cost, costliest first; then within a chunk all
+  // units of one head together (its query pairs share that head's K/V tiles
+  // in L2 while they run), costliest pair first.
+  sort_desc(p.pre_scratch, p.pre_seqs, n_chunks,
+            [&](int2 rec) {
+              const int2 r = row(rec.x);
+              int cost = 0;
+              for (int qp = 0; qp < rec.y; ++qp) cost += pair_cost(r.x, r.y, qp);
+              return cost;
             },
             bucket, warp_sums);
+  const int unit_cap = p.pre_cap * a.num_heads;
+  uint64_t unit_base = 0;
+  for (int c0 = 0; c0 < n_chunks; c0 += kPlanThreads) {
+    const int c = c0 + tid;
+    const int2 rec = c < n_chunks ? p.pre_seqs[c] : make_int2(0, 0);
+    const uint32_t n = c < n_chunks ? uint32_t(rec.y) * uint32_t(a.num_heads) : 0u;
+    uint64_t total;
+    const uint64_t off = unit_base + block_excl_scan(n, warp_sums, total);
+    unit_base += total;
+    if (n > 0) {
+      if (off + n <= uint64_t(unit_cap)) {
+        for (int h = 0; h < a.num_heads; ++h)
+          for (int k = 0; k < rec.y; ++k)
+            p.pre_units[off + uint64_t(h) * rec.y + k] = make_int2(rec.x, (rec.y - 1 - k) | (h << 16));
+      } else {
+        raise_error(a.err, kErrInvalid);
+      }
+    }
+  }
+  const int n_pre_units = int(unit_base < uint64_t(unit_cap) ? unit_base : uint64_t(unit_cap));
   if (tid == 0) {
     p.header[0] = n_dec;
-    p.header[1] = n_pre;
+    p.header[1] = n_pre_units;
     p.header[2] = 0;
     p.header[3] = 0;
     p.header[4] = int32_t(p.tag);
     p.header[5] = split;
+    p.header[6] = z.num_seqs;
+    p.header[7] = z.num_tokens;
   }
 }
 
@@ -222,7 +277,8 @@ size_t step_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_he
   const size_t pre_cap = T / kPrefillPairRows + (S < T / 2 ? S : T / 2) + 1;
   return 256 +                                                        // header
          2 * align256(S * splits * sizeof(int2)) +                    // decode items + scratch
-         2 * align256(pre_cap * sizeof(int2)) +                       // prefill items + scratch
+         2 * align256(pre_cap * sizeof(int2)) +                       // prefill chunk records + scratch
+         align256(pre_cap * num_heads * sizeof(int2)) +               // prefill units
          align256(S * num_heads * sizeof(int32_t)) +                  // tickets
          (splits > 1 ? S * num_heads * splits * (head_dim + 2) * sizeof(float) : 0);   // partials
 }
@@ -244,10 +300,12 @@ cb_status step_plan_layout(void* workspace, size_t workspace_bytes, int32_t num_
   w += align256(S * splits * sizeof(int2));
   plan->dec_scratch = reinterpret_cast<int2*>(w);
   w += align256(S * splits * sizeof(int2));
-  plan->pre_items = reinterpret_cast<int2*>(w);
+  plan->pre_seqs = reinterpret_cast<int2*>(w);
   w += align256(pre_cap * sizeof(int2));
   plan->pre_scratch = reinterpret_cast<int2*>(w);
   w += align256(pre_cap * sizeof(int2));
+  plan->pre_units = reinterpret_cast<int2*>(w);
+  w += align256(pre_cap * num_heads * sizeof(int2));
   plan->tickets = reinterpret_cast<int32_t*>(w);
   w += align256(S * num_heads * sizeof(int32_t));
   plan->partials = reinterpret_cast<float*>(w);

@@ -197,18 +197,21 @@ __device__ __forceinline__ void grid_dependency_wait() {
 }
 
 struct PrefillWork {
-  const int2* items;        // the plan's (sequence, query pair) items, costliest first
-  const int32_t* header;    // [1] = number of items
+  const int2* units;        // the plan's units (sequence, query pair | head << 16), in claim order
+  const int32_t* header;    // [1] = number of units
   int32_t* claims;          // claim counter
-  int32_t item_cap;         // capacity of the item list
+  int32_t unit_cap;         // capacity of the unit list
   uint32_t tag;             // the plan's call tag
 };
 
 // Persistent: a fixed grid of CTAs (one per SM) claims units until none are
-// left.  The K loader claims each unit and publishes it in a two-slot ring of
-// work items that the V loader, the MMA thread and the softmax warps read in
-// the same order; every barrier phase runs on across units, so the next
-// unit's K tiles and Q load overlap the end of the current one.
+// left, in the plan's order: costliest chunk first, head by head, so the
+// query pairs of one (sequence, head) run at the same time and share its K/V
+// tiles in L2.
+// The K loader claims each unit and publishes it in a two-slot ring of work
+// items that the V loader, the MMA thread and the softmax warps read in the
+// same order; every barrier phase runs on across units, so the next unit's K
+// tiles and Q load overlap the end of the current one.
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const PrefillWork w) {
@@ -222,6 +225,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int B = a.block_size;
   const int H = a.num_heads;
+
+  grid_dependency_wait();                          // the plan kernel has finished
+  const uint32_t seen_tag = uint32_t(__ldcg(w.header + 4));
+  int n_units = __ldcg(w.header + 1);
+  if (seen_tag != w.tag || n_units < 0 || n_units > w.unit_cap) {   // a list from another call: no work
+    if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(a.err, kErrInvalid);
+    n_units = 0;
+  }
+  if (int(blockIdx.x) >= n_units) return;          // no unit could be left for this CTA: skip the setup
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
@@ -254,14 +266,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gsm + kOffTmemSlot);
-  grid_dependency_wait();                          // the plan kernel has finished
-  const uint32_t seen_tag = uint32_t(__ldcg(w.header + 4));
-  int n_items = __ldcg(w.header + 1);
-  if (seen_tag != w.tag || n_items < 0 || n_items > w.item_cap) {   // a list from another call: no work
-    if (threadIdx.x == 0) raise_error(a.err, kErrInvalid);
-    n_items = 0;
-  }
-  const int n_units = n_items * H;
 
   // A reader's view of work item n: wait for it, copy it, release the slot.
   // `arrive`: this thread is its warp's (or role's) one arrival.
@@ -296,11 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         WorkItem it = {};
         it.u = atomicAdd(w.claims, 1);
         if (it.u < n_units) {
-          const int2 pi = __ldcg(w.items + it.u / H);
-          it.s = pi.x;
-          it.h = it.u % H;
-          it.row0 = pi.y * kPrefillPairRows;
-          bool bad = it.s < 0 || it.s >= a.num_seqs || pi.y < 0;
+          const int2 pu = __ldcg(w.units + it.u);
+          const int qp = pu.y & 0xFFFF;
+          it.s = pu.x;
+          it.h = pu.y >> 16;
+          it.row0 = qp * kPrefillPairRows;
+          bool bad = it.s < 0 || it.s >= a.num_seqs || it.h < 0 || it.h >= H;
           if (!bad) {
             it.c0 = __ldcg(a.cu_seqlens_q + it.s);
             it.q_len = __ldcg(a.cu_seqlens_q + it.s + 1) - it.c0;
@@ -719,10 +724,10 @@ cb_status launch_prefill_tc(const AttnArgs& a, const StepPlan& plan, bool after_
     g_attr_set[dev] = true;
   }
   PrefillWork w;
-  w.items = plan.pre_items;
+  w.units = plan.pre_units;
   w.header = plan.header;
   w.claims = plan.header + 3;
-  w.item_cap = plan.pre_cap;
+  w.unit_cap = plan.pre_cap * a.num_heads;
   w.tag = plan.tag;
   // one CTA per SM, never more than units could exist
   const int64_t max_units = int64_t(plan.pre_cap) * a.num_heads;

@@ -379,6 +379,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const 
     return;
   }
   const int n_units = n_items * H;
+  if (int(blockIdx.x) >= n_units) return;   // no unit could be left for this CTA
   const int split_keys = __ldcg(sa.header + 5);            // keys per split, chosen by the plan
   const T* kp = static_cast<const T*>(a.k_pool);
   const T* vp = static_cast<const T*>(a.v_pool);

@@ -128,6 +128,58 @@ cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Planned steps and CUDA-graph capture.
+ * Hugging Face blog "Continuous batching from first principles", section
+ * "Continuous batching": every layer of a step sees the same packed batch, and
+ * static shapes are what let a step be captured as a CUDA graph.  So the work
+ * lists are built once per step (cb_plan_step) and every layer's attention
+ * reuses them (cb_ragged_attention_planned); with `dims` set, every launch of
+ * a step has the same shape and arguments from step to step, so a step made
+ * of these calls can be captured once and replayed with new metadata.
+ *
+ *   dims  NULL, or device int32[4] = {num_seqs, num_tokens, max_q_len,
+ *         max_context_len} of the step.  When set, the host arguments of the
+ *         same names are CAPACITIES: the extents the metadata buffers, q, out,
+ *         k_new, v_new and slot_mapping are allocated for (block_tables is
+ *         [num_seqs capacity][max_blocks_per_seq]).  A step whose device sizes
+ *         exceed them sets CB_ERR_INVALID on the device word and runs empty.
+ *   Only bf16 caches with head_dim 128 and a block size that is a multiple of
+ *   16 are planned (CB_ERR_UNSUPPORTED otherwise).
+ *   Make one call of each outside stream capture first: it resolves
+ *   per-device state (the error word, kernel attributes, a second stream).
+ * ------------------------------------------------------------------------- */
+
+/* cb_append_kv with the token count read from dims[1] on the device;
+ * max_tokens bounds it (the extent of k_new, v_new and slot_mapping). */
+cb_status cb_append_kv_dims(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                            const int32_t* dims, int32_t max_tokens, const cb_kv_cache* cache,
+                            void* stream);
+
+/* Build the step's work lists in `workspace` (at least
+ * cb_attention_workspace_size(cache, num_seqs, num_tokens, max_context_len)
+ * bytes) from cu_seqlens_q and context_lens.  Reads only the metadata;
+ * cache supplies the shape (its pools may be NULL).  The lists stay valid
+ * until the metadata changes or the workspace is reused for anything else. */
+cb_status cb_plan_step(const cb_kv_cache* cache, const int32_t* cu_seqlens_q,
+                       const int32_t* context_lens, const int32_t* dims, int32_t num_seqs,
+                       int32_t num_tokens, int32_t max_blocks_per_seq, int32_t max_q_len,
+                       int32_t max_context_len, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* cb_ragged_attention over the plan that cb_plan_step built in `workspace`:
+ * same result, for any layer's q, cache pools and out.  cu_seqlens_q,
+ * context_lens, dims, the sizes, the cache shape and workspace_bytes must be
+ * the ones the plan was made with (CB_ERR_INVALID otherwise).  Calls over one
+ * plan must not overlap on the GPU (they share its claim counters). */
+cb_status cb_ragged_attention_planned(const void* q, const cb_kv_cache* cache,
+                                      const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                      const int32_t* block_tables, const int32_t* dims,
+                                      int32_t num_seqs, int32_t num_tokens,
+                                      int32_t max_blocks_per_seq, int32_t max_q_len,
+                                      int32_t max_context_len, float scale, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * cb_decode_attention_noalloc -- decode attention that allocates nothing.
  * The paper has no counterpart: this is a deployment variant of the decode
  * rows of cb_ragged_attention for callers that cannot allocate device memory

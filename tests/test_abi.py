@@ -63,18 +63,20 @@ def test_workspace_size_rules(native_lib):
 
     def bf16_step(S, T, max_ctx, H=32, A=128):
         # header + decode items and their unsorted copy [S*splits] + prefill
-        # items and their unsorted copy [T/256 + min(S, T/2) + 1] (int2 each)
-        # + tickets [S,H] + partials, all for the shortest split (512 keys)
+        # chunk records and their unsorted copy [T/256 + min(S, T/2) + 1] +
+        # prefill units [that * H] (int2 each) + tickets [S,H] + partials,
+        # all for the shortest split (512 keys)
         splits = (max_ctx + 511) // 512
         pre_cap = T // 256 + min(S, T // 2) + 1
         partials = S * H * splits * (A + 2) * 4 if splits > 1 else 0
-        return 256 + 2 * a256(S * splits * 8) + 2 * a256(pre_cap * 8) + a256(S * H * 4) + partials
+        return (256 + 2 * a256(S * splits * 8) + 2 * a256(pre_cap * 8) + a256(pre_cap * H * 8)
+                + a256(S * H * 4) + partials)
 
     # one split per row: no partials needed
-    assert native_lib.cb_attention_workspace_size(ctypes.byref(c), 8, 8, 512) == bf16_step(8, 8, 512) == 2304
+    assert native_lib.cb_attention_workspace_size(ctypes.byref(c), 8, 8, 512) == bf16_step(8, 8, 512) == 3584
     # decode rows with up to 9 splits: partials [S,H,splits,A+2] fp32 dominate
     n = native_lib.cb_attention_workspace_size(ctypes.byref(c), 256, 256, 4097)
-    assert n == bf16_step(256, 256, 4097) == 256 + 36864 + 2560 + 32768 + 256 * 32 * 9 * 130 * 4
+    assert n == bf16_step(256, 256, 4097) == 256 + 36864 + 2560 + 33280 + 32768 + 256 * 32 * 9 * 130 * 4
     c.dtype = native.CB_DTYPE_F32
     c.head_dim = 64
     n = native_lib.cb_attention_workspace_size(ctypes.byref(c), 3, 6, 1024)
