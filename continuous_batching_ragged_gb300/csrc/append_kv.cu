@@ -4,9 +4,9 @@
 // kernel": the new keys and values are written into the KV cache, each into
 // its own request's entry, before attention reads the cache back.
 //
-// A pure copy, HBM-bound: each thread moves one 16-byte chunk of one (token,
-// head) row of K or V.  Source reads are fully contiguous; a (token, head) row
-// of head_dim * elem bytes lands contiguously at pool[block][h][offset][:].
+// A pure copy, HBM-bound.  A token's K (and V) rows are contiguous in k_new;
+// a (token, head) row of head_dim * elem bytes lands contiguously at
+// pool[block][h][offset][:].
 #include <algorithm>
 
 #include "device_common.cuh"
@@ -14,43 +14,60 @@
 
 namespace {
 
-__global__ void __launch_bounds__(256) append_kv_kernel(
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;      // 16-byte chunks in flight per thread
+
+// One CTA per token (striding over tokens when the count comes from the
+// device): its slot is read once, then the CTA copies the token's K and V
+// rows, 2 * heads_x_chunks 16-byte chunks, kUnroll loads in flight per thread.
+__global__ void __launch_bounds__(kThreads) append_kv_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
     const int64_t* __restrict__ slot_mapping, uint4* __restrict__ k_pool,
-    uint4* __restrict__ v_pool, int64_t chunks_per_tensor, int32_t heads_x_chunks,
+    uint4* __restrict__ v_pool, int32_t num_tokens, int32_t heads_x_chunks,
     int32_t chunks_per_row, int32_t num_heads, int32_t block_size, int64_t num_slots,
     const int32_t* __restrict__ dims, unsigned* err) {
-  // dims: the step's token count comes from device memory (dims[1], at most
-  // the chunks_per_tensor the launch was sized for); the grid strides over it
-  int64_t per_tensor = chunks_per_tensor;
-  if (dims) {
+  int32_t T = num_tokens;
+  if (dims) {                   // the step's token count, at most num_tokens (the capacity)
     const int32_t t = dims[1];
-    const int64_t n = int64_t(t) * heads_x_chunks;
-    if (t < 0 || n > chunks_per_tensor) {
+    if (t < 0 || t > num_tokens) {
       if (blockIdx.x == 0 && threadIdx.x == 0) cb::raise_error(err, cb::kErrInvalid);
       return;
     }
-    per_tensor = n;
+    T = t;
   }
-  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < 2 * per_tensor;
-       idx += int64_t(gridDim.x) * blockDim.x) {
-    const bool is_v = idx >= per_tensor;
-    const int64_t i = is_v ? idx - per_tensor : idx;
-    const int64_t t = i / heads_x_chunks;
-    const int32_t rem = int32_t(i - t * heads_x_chunks);
-    const int32_t h = rem / chunks_per_row;
-    const int32_t c = rem - h * chunks_per_row;
-    const int64_t slot = slot_mapping[t];
+  const int32_t n = 2 * heads_x_chunks;
+  for (int32_t tok = blockIdx.x; tok < T; tok += gridDim.x) {
+    const int64_t slot = slot_mapping[tok];
     if (slot < 0) continue;
     if (slot >= num_slots) {
-      cb::raise_error(err, cb::kErrBounds);
+      if (threadIdx.x == 0) cb::raise_error(err, cb::kErrBounds);
       continue;
     }
     const int64_t blk = slot / block_size;
     const int64_t off = slot - blk * block_size;
-    const uint4 val = is_v ? cb::ldg_stream(v_new + i) : cb::ldg_stream(k_new + i);
-    uint4* pool = is_v ? v_pool : k_pool;
-    pool[((blk * num_heads + h) * block_size + off) * chunks_per_row + c] = val;
+    const uint4* ks = k_new + int64_t(tok) * heads_x_chunks;
+    const uint4* vs = v_new + int64_t(tok) * heads_x_chunks;
+    const int64_t dst0 = (blk * num_heads * block_size + off) * chunks_per_row;
+    const int64_t head_stride = int64_t(block_size) * chunks_per_row;
+    for (int32_t i0 = threadIdx.x; i0 < n; i0 += kThreads * kUnroll) {
+      uint4 val[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int32_t i = i0 + u * kThreads;
+        if (i < n) val[u] = i < heads_x_chunks ? cb::ldg_stream(ks + i) : cb::ldg_stream(vs + (i - heads_x_chunks));
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int32_t i = i0 + u * kThreads;
+        if (i < n) {
+          const bool is_v = i >= heads_x_chunks;
+          const int32_t r = is_v ? i - heads_x_chunks : i;
+          const int32_t h = r / chunks_per_row;
+          const int32_t c = r - h * chunks_per_row;
+          (is_v ? v_pool : k_pool)[dst0 + h * head_stride + c] = val[u];
+        }
+      }
+    }
   }
 }
 
@@ -76,18 +93,16 @@ cb_status append(const void* k_new, const void* v_new, const int64_t* slot_mappi
   if (!err) return CB_ERR_CUDA;
 
   const int32_t chunks_per_row = int32_t(row_bytes / 16);
+  if (int64_t(chunks_per_row) * cache->num_heads * 2 > 0x7FFFFFFF)
+    return cb::fail(CB_ERR_UNSUPPORTED, "%s: rows too wide", who);
   const int32_t heads_x_chunks = chunks_per_row * cache->num_heads;
-  const int64_t per_tensor = int64_t(num_tokens) * heads_x_chunks;
-  const int64_t threads = 2 * per_tensor;
-  const int block = 256;
-  int64_t grid = (threads + block - 1) / block;
-  // with device sizes the step may be far below the capacity: a grid of a few
-  // CTAs per SM strides over whatever the step holds
+  // one CTA per token; with device sizes the step may be far below the
+  // capacity, so a few CTAs per SM stride over whatever the step holds
+  int64_t grid = num_tokens;
   if (dims) grid = std::min<int64_t>(grid, int64_t(cb::sm_count()) * 8);
-  if (grid > 0x7FFFFFFF) return cb::fail(CB_ERR_INVALID, "%s: too many tokens", who);
-  append_kv_kernel<<<unsigned(grid), block, 0, static_cast<cudaStream_t>(stream)>>>(
+  append_kv_kernel<<<unsigned(grid), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
-      static_cast<uint4*>(cache->k), static_cast<uint4*>(cache->v), per_tensor, heads_x_chunks,
+      static_cast<uint4*>(cache->k), static_cast<uint4*>(cache->v), num_tokens, heads_x_chunks,
       chunks_per_row, cache->num_heads, cache->block_size,
       int64_t(cache->num_blocks) * cache->block_size, dims, err);
   cudaError_t e = cudaGetLastError();

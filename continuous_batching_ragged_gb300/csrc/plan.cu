@@ -26,7 +26,7 @@
 namespace cb {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;
 constexpr int kCostBuckets = 4096;     // costs at or above the last bucket share it
 constexpr int kUnitsPerCta = 6;        // decode units per persistent CTA the split size aims for
 constexpr int kRowCache = 2048;        // rows whose (q_len, ctx) stay in shared memory after pass 1
@@ -111,7 +111,7 @@ __device__ void sort_desc(const int2* in, int2* out, int n, Key key, uint32_t* b
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += kPlanThreads) atomicAdd(&bucket[min(key(in[i]), kCostBuckets - 1)], 1u);
   __syncthreads();
-  // descending order: thread t owns buckets kCostBuckets-1-4t .. kCostBuckets-4-4t
+  // descending order: thread t owns the kPer buckets just below kCostBuckets - kPer * t
   constexpr int kPer = kCostBuckets / kPlanThreads;
   uint32_t local[kPer], sum = 0;
 #pragma unroll
@@ -237,25 +237,30 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
             },
             bucket, warp_sums);
   const int unit_cap = p.pre_cap * a.num_heads;
-  uint64_t unit_base = 0;
+  uint64_t unit_base = 0;                   // first unit of each sorted chunk, into pre_scratch[].x
   for (int c0 = 0; c0 < n_chunks; c0 += kPlanThreads) {
     const int c = c0 + tid;
-    const int2 rec = c < n_chunks ? p.pre_seqs[c] : make_int2(0, 0);
-    const uint32_t n = c < n_chunks ? uint32_t(rec.y) * uint32_t(a.num_heads) : 0u;
+    const uint32_t n = c < n_chunks ? uint32_t(p.pre_seqs[c].y) * uint32_t(a.num_heads) : 0u;
     uint64_t total;
     const uint64_t off = unit_base + block_excl_scan(n, warp_sums, total);
     unit_base += total;
-    if (n > 0) {
-      if (off + n <= uint64_t(unit_cap)) {
-        for (int h = 0; h < a.num_heads; ++h)
-          for (int k = 0; k < rec.y; ++k)
-            p.pre_units[off + uint64_t(h) * rec.y + k] = make_int2(rec.x, (rec.y - 1 - k) | (h << 16));
-      } else {
-        raise_error(a.err, kErrInvalid);
-      }
-    }
+    if (c < n_chunks) p.pre_scratch[c] = make_int2(off < uint64_t(unit_cap) ? int(off) : unit_cap, 0);
   }
+  if (unit_base > uint64_t(unit_cap) && tid == 0) raise_error(a.err, kErrInvalid);
   const int n_pre_units = int(unit_base < uint64_t(unit_cap) ? unit_base : uint64_t(unit_cap));
+  __syncthreads();
+  // every thread writes units: unit i belongs to the last chunk starting at or before it
+  for (int i = tid; i < n_pre_units; i += kPlanThreads) {
+    int lo = 0, hi = n_chunks - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.pre_scratch[mid].x <= i) lo = mid; else hi = mid - 1;
+    }
+    const int2 rec = p.pre_seqs[lo];
+    const int local = i - p.pre_scratch[lo].x;
+    const int h = local / rec.y, k = local - h * rec.y;
+    p.pre_units[i] = make_int2(rec.x, (rec.y - 1 - k) | (h << 16));
+  }
   if (tid == 0) {
     p.header[0] = n_dec;
     p.header[1] = n_pre_units;
