@@ -251,7 +251,8 @@ def time_oracle(b, budget_s: float):
 # ---------------------------------------------------------------------------
 
 def run_trace_graph(torch, api, W, requests, *, num_layers, num_heads, head_dim, block_size,
-                    token_budget, num_blocks, seed, max_steps=100000):
+                    token_budget, num_blocks, seed, max_steps=100000, admission="reserve_lifetime",
+                    stats_out=None):
     """run_trace with each step captured once as a CUDA graph (StepGraph):
     per step the host builds the batch, the device generator writes every
     layer's Q/K/V (not timed), the metadata is copied into the graph's fixed
@@ -270,7 +271,7 @@ def run_trace_graph(torch, api, W, requests, *, num_layers, num_heads, head_dim,
     out = [torch.zeros(shape, dtype=dt, device="cuda")]
     sg = StepGraph(caches, q, k, v, out, max_seqs=token_budget, max_blocks_per_seq=max_blocks,
                    scale=1.0 / math.sqrt(head_dim))
-    sched = api.Scheduler(token_budget, block_size, num_blocks)
+    sched = api.Scheduler(token_budget, block_size, num_blocks, admission=admission)
     for r in requests:
         sched.add_request(r.id, r.arrival_step, r.prompt_len, r.output_len)
     steps = []
@@ -312,13 +313,17 @@ def run_trace_graph(torch, api, W, requests, *, num_layers, num_heads, head_dim,
         steps.append({"T": T, "S": S, "decode": bt.num_decode, "sched_s": t_sched,
                       "gpu_ms": e0.elapsed_time(e1), "kv_tokens": int(np.sum(bt.context_lens)),
                       "q_lens": bt.q_lens, "max_q_len": bt.max_q_len, "ctx": bt.context_lens})
+    if stats_out is not None:
+        st = sched.stats()
+        stats_out.update(num_preempted=st.num_preempted, recomputed_tokens=st.recomputed_tokens)
     del sg, caches
     torch.cuda.empty_cache()
     return steps
 
 
 def run_trace(torch, api, W, requests, *, num_layers, num_heads, head_dim, block_size,
-              token_budget, num_blocks, seed, on_layer=None, max_steps=100000):
+              token_budget, num_blocks, seed, on_layer=None, max_steps=100000,
+              admission="reserve_lifetime", stats_out=None):
     """Serve ``requests`` to completion.  Each step: cb_build_batch on the host,
     metadata to the device, then per layer the step's Q/K/V (device generator,
     keyed by request id and position, not timed) followed by the timed
@@ -330,7 +335,7 @@ def run_trace(torch, api, W, requests, *, num_layers, num_heads, head_dim, block
     for c in caches:
         c.k.zero_()
         c.v.zero_()
-    sched = api.Scheduler(token_budget, block_size, num_blocks)
+    sched = api.Scheduler(token_budget, block_size, num_blocks, admission=admission)
     for r in requests:
         sched.add_request(r.id, r.arrival_step, r.prompt_len, r.output_len)
     scale = 1.0 / math.sqrt(head_dim)
@@ -391,6 +396,9 @@ def run_trace(torch, api, W, requests, *, num_layers, num_heads, head_dim, block
                       "kv_tokens": int(np.sum(bt.context_lens)), "q_lens": q_lens,
                       "max_q_len": bt.max_q_len,
                       "ctx": bt.context_lens})
+    if stats_out is not None:
+        st = sched.stats()
+        stats_out.update(num_preempted=st.num_preempted, recomputed_tokens=st.recomputed_tokens)
     del caches
     torch.cuda.empty_cache()
     return steps
@@ -484,17 +492,21 @@ def run_trace_bench(args, graph=False):
     """The serving trace end to end: 2000 requests, 32 layers, budget 4096
     (graph: each step one CUDA-graph replay)."""
     from continuous_batching_ragged_gb300 import workloads as W
-    cfg = W.SERVING_TRACE
+    cfg = dict(W.SERVING_TRACE)
+    if args.trace_blocks:
+        cfg["num_blocks"] = args.trace_blocks
     reqs = W.serving_trace()
     label = (f"serving_trace_{len(reqs)}req_{cfg['num_layers']}layers_m{cfg['token_budget']}_"
              f"{cfg['num_blocks']}blocks_bf16_H32_A128_B16")
+    if args.admission != "reserve_lifetime":
+        label += "_" + args.admission
     rank, world, local = dist_info()
     if args.impl == "reference":
         if rank != 0:
             return
         # the oracle on one mid-trace step's batch (one layer), as a bounded sample
         from oracle.scheduler import Scheduler as OS
-        o = OS(cfg["token_budget"], cfg["block_size"], cfg["num_blocks"])
+        o = OS(cfg["token_budget"], cfg["block_size"], cfg["num_blocks"], admission=args.admission)
         for r in reqs:
             o.add_request(r.id, r.arrival_step, r.prompt_len, r.output_len)
         batch = None
@@ -518,12 +530,14 @@ def run_trace_bench(args, graph=False):
               block_size=cfg["block_size"], token_budget=cfg["token_budget"],
               num_blocks=cfg["num_blocks"], seed=4)
     runner = run_trace_graph if graph else run_trace
+    kw["admission"] = args.admission
     # warm-up: a short trace of the first requests
     runner(torch, api, W, reqs[:16], max_steps=max(3, args.warmup), **kw)
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     t0 = time.perf_counter()
-    steps = runner(torch, api, W, reqs, **kw)
+    sched_stats = {}
+    steps = runner(torch, api, W, reqs, stats_out=sched_stats, **kw)
     wall = time.perf_counter() - t0
     clocks = sampler.stop()
     busy = [st for st in steps if st["T"] > 0]
@@ -547,6 +561,10 @@ def run_trace_bench(args, graph=False):
                               "frac_p90": float(np.percentile(fracs, 90)),
                               "bytes_total": sum(r[1] for r in roof), "flops_total": sum(r[2] for r in roof)},
             "scheduler_us_per_step": sched_us, "wall_s": wall,
+            "admission": args.admission, "preemptions": sched_stats.get("num_preempted", 0),
+            "recomputed_tokens": sched_stats.get("recomputed_tokens", 0),
+            "useful_tokens_per_s": (tokens - sched_stats.get("recomputed_tokens", 0)) / (gpu_ms * 1e-3),
+            "gpu_ms_total": gpu_ms,
             "mean_decode_per_step": float(np.mean([st["decode"] for st in busy])),
             "clocks": clocks,
             "gpu_launches": (sum(1 + 3 * cfg["num_layers"] for st in busy) if graph else
@@ -568,6 +586,9 @@ def main():
                                                              "mixed_padded", "insertion", "insertion_padded"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--admission", default="reserve_lifetime", choices=["reserve_lifetime", "prompt_preempt"],
+                    help="scheduler admission policy of the trace workloads")
+    ap.add_argument("--trace-blocks", type=int, default=0, help="KV pool blocks of the trace workloads")
     ap.add_argument("--decode-seqs", type=int, default=256,
                     help="sequences of the decode workload (smaller cases for profiling)")
     args = ap.parse_args()

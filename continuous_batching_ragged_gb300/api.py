@@ -203,6 +203,7 @@ class Batch:
     slot_mapping: np.ndarray
     request_ids: np.ndarray
     evicted_ids: np.ndarray
+    preempted_ids: np.ndarray
 
     @property
     def num_seqs(self) -> int:
@@ -226,9 +227,11 @@ def _arr(ptr, n, dtype):
 class Scheduler:
     """cb_scheduler_* on the host (no GPU needed)."""
 
-    def __init__(self, token_budget: int, block_size: int, num_blocks: int, max_num_seqs: int = 0):
+    def __init__(self, token_budget: int, block_size: int, num_blocks: int, max_num_seqs: int = 0,
+                 admission: str = "reserve_lifetime"):
         self._L = native.lib()
-        cfg = native.cb_sched_config(token_budget, block_size, num_blocks, max_num_seqs)
+        cfg = native.cb_sched_config(token_budget, block_size, num_blocks, max_num_seqs,
+                                     native.ADMISSION[admission])
         h = ctypes.c_void_p()
         check(self._L.cb_scheduler_create(ctypes.byref(cfg), ctypes.byref(h)), "cb_scheduler_create")
         self._h = h
@@ -252,7 +255,8 @@ class Scheduler:
                      block_tables=_arr(b.block_tables, S * W, np.int32).reshape(S, W),
                      slot_mapping=_arr(b.slot_mapping, T, np.int64),
                      request_ids=_arr(b.request_ids, S, np.int64),
-                     evicted_ids=_arr(b.evicted_ids, b.num_evicted, np.int64))
+                     evicted_ids=_arr(b.evicted_ids, b.num_evicted, np.int64),
+                     preempted_ids=_arr(b.preempted_ids, b.num_preempted, np.int64))
 
     def complete_step(self) -> None:
         check(self._L.cb_complete_step(self._h), "cb_complete_step")

@@ -29,6 +29,7 @@ struct Request {
   int64_t arrival;
   int32_t prompt_len;
   int32_t output_len;
+  int32_t prefill_len = 0; // tokens of the next prefill: the prompt, or after a preemption every known token
   int32_t computed = 0;    // tokens whose K/V is in the cache
   int32_t generated = 0;   // output tokens produced so far
   int32_t reserved = 0;    // blocks reserved at admission
@@ -59,9 +60,31 @@ struct cb_scheduler {
   std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_blocks;
   std::vector<Chosen> pending;
   bool has_pending = false;
+  int64_t num_preempted = 0;
+  int64_t recomputed_tokens = 0;
   // output arrays of the last cb_build_batch
   std::vector<int32_t> cu, ctx, bt;
-  std::vector<int64_t> slots, ids, evicted;
+  std::vector<int64_t> slots, ids, evicted, preempted;
+
+  // CB_ADMIT_PROMPT_PREEMPT: give `r`'s blocks back and return it to the
+  // waiting queue; its next prefill recomputes every token it knows.
+  void preempt(Request* r) {
+    for (int32_t b : r->blocks) free_blocks.push(b);
+    r->blocks.clear();
+    recomputed_tokens += r->computed;
+    r->computed = 0;
+    r->prefill_len = r->prompt_len + r->generated;
+    waiting.emplace(r->arrival, r->id);
+    preempted.push_back(r->id);
+    ++num_preempted;
+  }
+  // take `n` blocks, lowest ids first
+  void take_blocks(Request* r, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) {
+      r->blocks.push_back(free_blocks.top());
+      free_blocks.pop();
+    }
+  }
 };
 
 extern "C" cb_status cb_scheduler_create(const cb_sched_config* config, cb_scheduler** out) {
@@ -70,6 +93,8 @@ extern "C" cb_status cb_scheduler_create(const cb_sched_config* config, cb_sched
       config->max_num_seqs < 0)
     return cb::fail(CB_ERR_INVALID, "cb_scheduler_create: token_budget, block_size and num_blocks "
                                     "must be >= 1 and max_num_seqs >= 0");
+  if (config->admission != CB_ADMIT_RESERVE_LIFETIME && config->admission != CB_ADMIT_PROMPT_PREEMPT)
+    return cb::fail(CB_ERR_INVALID, "cb_scheduler_create: unknown admission policy %d", config->admission);
   cb_scheduler* s = new (std::nothrow) cb_scheduler();
   if (!s) return cb::fail(CB_ERR_INVALID, "cb_scheduler_create: out of host memory");
   s->cfg = *config;
@@ -92,6 +117,7 @@ extern "C" cb_status cb_add_request(cb_scheduler* s, int64_t id, int64_t arrival
   r.arrival = arrival_step;
   r.prompt_len = prompt_len;
   r.output_len = output_len;
+  r.prefill_len = prompt_len;
   if (blocks_needed(r, s->cfg.block_size) > s->cfg.num_blocks)
     return cb::fail(CB_ERR_NO_BLOCKS, "cb_add_request: request %lld needs more blocks than the pool",
                     (long long)id);
@@ -122,35 +148,70 @@ extern "C" cb_status cb_build_batch(cb_scheduler* s, cb_batch* out) {
   }
   s->running.swap(still);
 
-  // 2. admit the FIFO head while it has arrived and fits
-  while (!s->waiting.empty()) {
-    auto head = *s->waiting.begin();
-    Request& r = s->all.at(head.second);
-    if (r.arrival > s->step) break;
-    if (s->cfg.max_num_seqs > 0 && int32_t(s->running.size()) >= s->cfg.max_num_seqs) break;
-    int64_t need = blocks_needed(r, B);
-    if (int64_t(s->cfg.num_blocks) - s->reserved_total < need) break;
-    s->waiting.erase(s->waiting.begin());
-    r.reserved = int32_t(need);
-    s->reserved_total += need;
-    s->running.push_back(&r);
-  }
-
-  // 3. decode requests first, one token each, 4. then prefill chunks
+  const bool preempting = s->cfg.admission == CB_ADMIT_PROMPT_PREEMPT;
+  s->preempted.clear();
   s->pending.clear();
   int32_t room = s->cfg.token_budget;
-  for (Request* r : s->running) {
-    if (room == 0) break;
-    if (r->computed >= r->prompt_len) {
+  // 2. admit the FIFO head while it has arrived and fits
+  auto admit = [&]() {
+    while (!s->waiting.empty()) {
+      auto head = *s->waiting.begin();
+      Request& r = s->all.at(head.second);
+      if (r.arrival > s->step) break;
+      if (s->cfg.max_num_seqs > 0 && int32_t(s->running.size()) >= s->cfg.max_num_seqs) break;
+      if (preempting) {
+        // the prefill's blocks, taken now
+        const int64_t need = (int64_t(r.prefill_len) + B - 1) / B;
+        if (int64_t(s->free_blocks.size()) < need) break;
+        s->waiting.erase(s->waiting.begin());
+        s->take_blocks(&r, need);
+      } else {
+        const int64_t need = blocks_needed(r, B);
+        if (int64_t(s->cfg.num_blocks) - s->reserved_total < need) break;
+        s->waiting.erase(s->waiting.begin());
+        r.reserved = int32_t(need);
+        s->reserved_total += need;
+      }
+      s->running.push_back(&r);
+    }
+  };
+  // 3. decode requests first, one token each
+  auto choose_decodes = [&]() {
+    for (size_t i = 0; i < s->running.size() && room > 0; ++i) {
+      Request* r = s->running[i];
+      if (r->computed < r->prefill_len) continue;
+      if (preempting && r->computed / B >= int32_t(r->blocks.size())) {
+        // this token enters a new block: free one by preempting the latest admitted
+        while (s->free_blocks.empty() && s->running.back() != r) {
+          s->preempt(s->running.back());
+          s->running.pop_back();
+        }
+        if (s->free_blocks.empty()) {           // r is the latest admitted: it goes itself
+          s->preempt(r);
+          s->running.pop_back();
+          break;
+        }
+        s->take_blocks(r, 1);
+      }
       s->pending.push_back({r, 1, true});
       --room;
     }
+  };
+  if (preempting) {
+    // running requests take their blocks before anyone is admitted, and a step
+    // that had to preempt admits no one
+    choose_decodes();
+    if (s->preempted.empty()) admit();
+  } else {
+    admit();
+    choose_decodes();
   }
   const int32_t num_decode = int32_t(s->pending.size());
+  // 4. then prefill chunks, greedily in admission order
   for (Request* r : s->running) {
     if (room == 0) break;
-    if (r->computed < r->prompt_len) {
-      int32_t n = std::min(r->prompt_len - r->computed, room);
+    if (r->computed < r->prefill_len) {
+      int32_t n = std::min(r->prefill_len - r->computed, room);
       s->pending.push_back({r, n, false});
       room -= n;
     }
@@ -169,9 +230,9 @@ extern "C" cb_status cb_build_batch(cb_scheduler* s, cb_batch* out) {
     for (int32_t k = 0; k < c.n; ++k) {
       int32_t pos = r->computed + k;
       if (pos / B >= int32_t(r->blocks.size())) {
-        // The admission reservation guarantees a free block exists.
-        r->blocks.push_back(s->free_blocks.top());
-        s->free_blocks.pop();
+        // reserve-lifetime admission guarantees a free block exists (with
+        // preemption every block is already taken)
+        s->take_blocks(r, 1);
       }
       s->slots.push_back(int64_t(r->blocks[pos / B]) * B + pos % B);
     }
@@ -202,6 +263,8 @@ extern "C" cb_status cb_build_batch(cb_scheduler* s, cb_batch* out) {
   out->request_ids = s->ids.data();
   out->num_evicted = int32_t(s->evicted.size());
   out->evicted_ids = s->evicted.data();
+  out->num_preempted = int32_t(s->preempted.size());
+  out->preempted_ids = s->preempted.data();
   return CB_OK;
 }
 
@@ -210,7 +273,7 @@ extern "C" cb_status cb_complete_step(cb_scheduler* s) {
   if (!s->has_pending) return cb::fail(CB_ERR_INVALID, "cb_complete_step: no batch was built");
   for (Chosen& c : s->pending) {
     c.req->computed += c.n;
-    if (c.decode || c.req->computed == c.req->prompt_len) c.req->generated += 1;
+    if (c.decode || c.req->computed == c.req->prefill_len) c.req->generated += 1;
   }
   s->pending.clear();
   s->has_pending = false;
@@ -226,5 +289,7 @@ extern "C" cb_status cb_scheduler_stats(const cb_scheduler* s, cb_sched_stats* o
   out->free_blocks = int32_t(s->free_blocks.size());
   out->reserved_blocks = int32_t(s->reserved_total);
   out->num_finished = s->finished;
+  out->num_preempted = s->num_preempted;
+  out->recomputed_tokens = s->recomputed_tokens;
   return CB_OK;
 }

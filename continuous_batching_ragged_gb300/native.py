@@ -26,6 +26,11 @@ EXPORTS = ("cb_append_kv", "cb_attention_workspace_size", "cb_ragged_attention",
            "cb_synth_tokens", "cb_synth_fill_cache", "cb_selftest_bounded_wait")
 
 
+CB_ADMIT_RESERVE_LIFETIME = 0
+CB_ADMIT_PROMPT_PREEMPT = 1
+ADMISSION = {"reserve_lifetime": CB_ADMIT_RESERVE_LIFETIME, "prompt_preempt": CB_ADMIT_PROMPT_PREEMPT}
+
+
 class cb_kv_cache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_blocks", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("num_heads", ctypes.c_int32),
@@ -34,7 +39,8 @@ class cb_kv_cache(ctypes.Structure):
 
 class cb_sched_config(ctypes.Structure):
     _fields_ = [("token_budget", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("num_blocks", ctypes.c_int32), ("max_num_seqs", ctypes.c_int32)]
+                ("num_blocks", ctypes.c_int32), ("max_num_seqs", ctypes.c_int32),
+                ("admission", ctypes.c_int32)]
 
 
 _P32 = ctypes.POINTER(ctypes.c_int32)
@@ -47,13 +53,14 @@ class cb_batch(ctypes.Structure):
                 ("max_q_len", ctypes.c_int32), ("max_context_len", ctypes.c_int32),
                 ("cu_seqlens_q", _P32), ("context_lens", _P32), ("block_tables", _P32),
                 ("slot_mapping", _P64), ("request_ids", _P64), ("num_evicted", ctypes.c_int32),
-                ("evicted_ids", _P64)]
+                ("evicted_ids", _P64), ("num_preempted", ctypes.c_int32), ("preempted_ids", _P64)]
 
 
 class cb_sched_stats(ctypes.Structure):
     _fields_ = [("step", ctypes.c_int64), ("num_waiting", ctypes.c_int32),
                 ("num_running", ctypes.c_int32), ("free_blocks", ctypes.c_int32),
-                ("reserved_blocks", ctypes.c_int32), ("num_finished", ctypes.c_int64)]
+                ("reserved_blocks", ctypes.c_int32), ("num_finished", ctypes.c_int64),
+                ("num_preempted", ctypes.c_int64), ("recomputed_tokens", ctypes.c_int64)]
 
 
 _lib = None

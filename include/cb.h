@@ -227,12 +227,38 @@ cb_status cb_decode_attention_noalloc(const void* q, const cb_kv_cache* cache,
  * admission order; blocks are handed out lowest free id first; a request is
  * finished after output_len tokens (the prefill pass yields the first) and is
  * evicted at the start of the next cb_build_batch.
+ *
+ * Preemption (CB_ADMIT_PROMPT_PREEMPT).  hassanahmed.net, the paragraph on the
+ * memory manager under continuous batching: when the card fills, a request
+ * is evicted for a while and brought back later.  Read here as preemption by
+ * recompute, with these rules:
+ *   - The head of the queue is admitted when the free blocks cover its prefill.
+ *     Those blocks are taken at once (lowest ids first).
+ *   - When a decode token of request r needs a new block and none is free,
+ *     the most recently admitted running request is preempted, repeatedly,
+ *     until a block is free (r itself last).
+ *   - A preempted request gives back all its blocks and keeps the output
+ *     tokens it has produced. It rejoins the waiting queue at its original
+ *     (arrival_step, id) place, which is the head, since admission is FIFO.
+ *   - Its next prefill covers prompt_len + generated tokens, all of its known
+ *     tokens, and yields its next output token.
+ * The preempted ids of a step are reported in its batch.
  * ------------------------------------------------------------------------- */
+typedef enum {
+  /* reserve ceil((prompt_len + output_len) / block_size) blocks at admission:
+   * a running request never runs short and is never preempted */
+  CB_ADMIT_RESERVE_LIFETIME = 0,
+  /* take the prompt's blocks at admission and one more block whenever a
+   * decode token enters a new block; when none is free, preempt (below) */
+  CB_ADMIT_PROMPT_PREEMPT = 1
+} cb_admission;
+
 typedef struct {
   int32_t token_budget;   /* m = max tokens per step (max_num_batched_tokens) */
   int32_t block_size;
   int32_t num_blocks;
   int32_t max_num_seqs;   /* 0 = unlimited */
+  int32_t admission;      /* cb_admission; 0 (zero-initialised) = reserve the lifetime */
 } cb_sched_config;
 
 typedef struct cb_scheduler cb_scheduler;
@@ -253,6 +279,8 @@ typedef struct {
   const int64_t* request_ids;   /* [num_seqs] */
   int32_t num_evicted;
   const int64_t* evicted_ids;   /* [num_evicted], evicted by this call */
+  int32_t num_preempted;
+  const int64_t* preempted_ids; /* [num_preempted], preempted by this call (back to waiting) */
 } cb_batch;
 
 typedef struct {
@@ -262,6 +290,8 @@ typedef struct {
   int32_t free_blocks;
   int32_t reserved_blocks;
   int64_t num_finished;         /* evicted so far */
+  int64_t num_preempted;        /* preemptions so far */
+  int64_t recomputed_tokens;    /* prefill tokens spent re-computing preempted requests */
 } cb_sched_stats;
 
 cb_status cb_scheduler_create(const cb_sched_config* config, cb_scheduler** out);

@@ -30,6 +30,22 @@ Readings where the pages leave the step open:
 * the batch lists decode sequences first, then prefill chunks;
 * a request is finished when it has produced output_len tokens; it is evicted
   (its blocks freed) at the start of the next step.
+
+Admission with preemption (admission="prompt_preempt"), hassanahmed.net, the
+paragraph on the memory manager under continuous batching: when the card
+fills, a request is evicted temporarily and brought back later.  Read as
+preemption by recompute:
+
+* the head is admitted when the free blocks cover its prefill, and those
+  blocks are taken at once, lowest ids first;
+* running requests take their decode blocks before anyone is admitted: when a
+  decode token enters a new block and none is free, the most recently admitted
+  running request is preempted, repeatedly, the decoding request itself last;
+  a step that preempted admits no one;
+* a preempted request gives back all its blocks, keeps the output tokens it
+  produced, and rejoins the waiting queue at its (arrival, id) place -- the
+  head, admission being FIFO; its next prefill covers prompt + generated
+  tokens (every token it knows) and yields its next output token.
 """
 from __future__ import annotations
 
@@ -47,6 +63,7 @@ class _Req:
     arrival: int
     prompt_len: int
     output_len: int
+    prefill_len: int = 0       # tokens of the next prefill (the prompt, or all known after preemption)
     computed: int = 0          # tokens whose K/V is in the cache
     generated: int = 0         # output tokens produced
     blocks: list = dataclasses.field(default_factory=list)
@@ -63,6 +80,7 @@ class Batch:
     slot_mapping: np.ndarray   # [T] int64
     evicted_ids: np.ndarray    # [E] int64
     num_decode: int
+    preempted_ids: np.ndarray = dataclasses.field(default_factory=lambda: np.zeros(0, np.int64))
 
     @property
     def num_seqs(self) -> int:
@@ -74,9 +92,15 @@ class Batch:
 
 
 class Scheduler:
-    def __init__(self, token_budget: int, block_size: int, num_blocks: int, max_num_seqs: int = 0):
+    def __init__(self, token_budget: int, block_size: int, num_blocks: int, max_num_seqs: int = 0,
+                 admission: str = "reserve_lifetime"):
         if token_budget < 1 or block_size < 1 or num_blocks < 1 or max_num_seqs < 0:
             raise ValueError("bad scheduler config")
+        if admission not in ("reserve_lifetime", "prompt_preempt"):
+            raise ValueError("unknown admission policy")
+        self.preempting = admission == "prompt_preempt"
+        self.num_preempted = 0
+        self.recomputed_tokens = 0
         self.m = token_budget
         self.B = block_size
         self.NB = num_blocks
@@ -94,14 +118,28 @@ class Scheduler:
         return math.ceil((r.prompt_len + r.output_len) / self.B)
 
     def add_request(self, rid: int, arrival_step: int, prompt_len: int, output_len: int) -> None:
-        r = _Req(rid, arrival_step, prompt_len, output_len)
+        r = _Req(rid, arrival_step, prompt_len, output_len, prefill_len=prompt_len)
         if prompt_len < 1 or output_len < 1 or arrival_step < 0 or self._need(r) > self.NB:
             raise ValueError("request can never be admitted")
-        key = (arrival_step, rid)
+        self._enqueue(r)
+
+    def _enqueue(self, r: _Req) -> None:
+        key = (r.arrival, r.id)
         i = len(self.waiting)
         while i > 0 and (self.waiting[i - 1].arrival, self.waiting[i - 1].id) > key:
             i -= 1
         self.waiting.insert(i, r)
+
+    def _preempt(self, r: _Req, preempted: list) -> None:
+        for b in r.blocks:
+            heapq.heappush(self.free, b)
+        r.blocks = []
+        self.recomputed_tokens += r.computed
+        r.computed = 0
+        r.prefill_len = r.prompt_len + r.generated
+        self._enqueue(r)
+        preempted.append(r.id)
+        self.num_preempted += 1
 
     def build_batch(self) -> Batch:
         if self._pending is not None:
@@ -119,31 +157,62 @@ class Scheduler:
             else:
                 keep.append(r)
         self.running = keep
-        # 2. admit from the FIFO head while it fits
-        while self.waiting:
-            r = self.waiting[0]
-            if r.arrival > self.step:
-                break
-            if self.max_num_seqs and len(self.running) >= self.max_num_seqs:
-                break
-            need = self._need(r)
-            if self.NB - self.reserved_total < need:
-                break
-            self.waiting.pop(0)
-            r.reserved = need
-            self.reserved_total += need
-            self.running.append(r)
-        # 3. decode requests first, one token each; 4. then prefill chunks
         room = self.m
         chosen = []                       # (request, n_tokens, is_decode)
-        for r in self.running:
-            if r.computed >= r.prompt_len and room > 0:
+        preempted = []
+
+        def admit():                      # 2. admit from the FIFO head while it fits
+            while self.waiting:
+                r = self.waiting[0]
+                if r.arrival > self.step:
+                    break
+                if self.max_num_seqs and len(self.running) >= self.max_num_seqs:
+                    break
+                if self.preempting:
+                    need = math.ceil(r.prefill_len / self.B)
+                    if len(self.free) < need:
+                        break
+                    self.waiting.pop(0)
+                    r.blocks = [heapq.heappop(self.free) for _ in range(need)]
+                else:
+                    need = self._need(r)
+                    if self.NB - self.reserved_total < need:
+                        break
+                    self.waiting.pop(0)
+                    r.reserved = need
+                    self.reserved_total += need
+                self.running.append(r)
+
+        def choose_decodes():             # 3. decode requests first, one token each
+            nonlocal room
+            i = 0
+            while i < len(self.running) and room > 0:
+                r = self.running[i]
+                i += 1
+                if r.computed < r.prefill_len:
+                    continue
+                if self.preempting and r.computed // self.B >= len(r.blocks):
+                    while not self.free and self.running[-1] is not r:
+                        self._preempt(self.running.pop(), preempted)
+                    if not self.free:
+                        self._preempt(self.running.pop(), preempted)
+                        break
+                    r.blocks.append(heapq.heappop(self.free))
                 chosen.append((r, 1, True))
                 room -= 1
+
+        if self.preempting:
+            choose_decodes()
+            if not preempted:
+                admit()
+        else:
+            admit()
+            choose_decodes()
         num_decode = len(chosen)
+        # 4. then prefill chunks, greedily in admission order
         for r in self.running:
-            if r.computed < r.prompt_len and room > 0:
-                n = min(r.prompt_len - r.computed, room)
+            if r.computed < r.prefill_len and room > 0:
+                n = min(r.prefill_len - r.computed, room)
                 chosen.append((r, n, False))
                 room -= n
         # 5. blocks for the new positions, 6. metadata
@@ -167,14 +236,14 @@ class Scheduler:
         return Batch(request_ids=np.array([r.id for r, _, _ in chosen], dtype=np.int64),
                      q_lens=q_lens, cu_seqlens_q=cu, context_lens=ctx, block_tables=bt,
                      slot_mapping=slots, evicted_ids=np.array(evicted, dtype=np.int64),
-                     num_decode=num_decode)
+                     num_decode=num_decode, preempted_ids=np.array(preempted, dtype=np.int64))
 
     def complete_step(self) -> None:
         if self._pending is None:
             raise RuntimeError("no batch to complete")
         for r, n, is_decode in self._pending:
             r.computed += n
-            if is_decode or r.computed == r.prompt_len:
+            if is_decode or r.computed == r.prefill_len:
                 r.generated += 1
         self._pending = None
         self.step += 1

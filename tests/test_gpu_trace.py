@@ -12,7 +12,8 @@ from continuous_batching_ragged_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _run_and_check(reqs, *, num_layers, num_blocks, token_budget, check_every, seed=4):
+def _run_and_check(reqs, *, num_layers, num_blocks, token_budget, check_every, seed=4,
+                   admission="reserve_lifetime", stats_out=None):
     from continuous_batching_ragged_gb300 import api
     from gpu_harness import assert_tolerance, oracle_rows
     rng = np.random.default_rng(0)
@@ -32,8 +33,9 @@ def _run_and_check(reqs, *, num_layers, num_blocks, token_budget, check_every, s
 
     steps = bench.run_trace(torch, api, W, reqs, num_layers=num_layers, num_heads=32, head_dim=128,
                             block_size=16, token_budget=token_budget, num_blocks=num_blocks,
-                            seed=seed, on_layer=on_layer)
-    assert sum(st["T"] for st in steps) == sum(r.prompt_len + r.output_len - 1 for r in reqs)
+                            seed=seed, on_layer=on_layer, admission=admission, stats_out=stats_out)
+    recomputed = stats_out["recomputed_tokens"] if stats_out is not None else 0
+    assert sum(st["T"] for st in steps) == sum(r.prompt_len + r.output_len - 1 for r in reqs) + recomputed
     got, exp = [], []
     for layer, rid, c, q, rows, h, g in samples:
         b = W.RaggedBatch(num_heads=32, head_dim=128, block_size=16, dtype="bf16", seed=seed,
@@ -60,3 +62,16 @@ def test_serving_trace_full_size(native_lib):
                            num_blocks=cfg["num_blocks"], token_budget=cfg["token_budget"],
                            check_every=199)
     assert len(steps) > 100
+
+
+def test_serving_trace_with_preemption(native_lib):
+    """A pool too small for every admitted request to finish: with admission
+    reserving only the prefill, requests are preempted and recomputed.  The
+    recomputed keys and values are the same (they are a function of request
+    and position), so sampled rows still match the oracle's own history."""
+    reqs = W.serving_trace(num_requests=120, prompt_median=200, prompt_cap=2048, out_median=30,
+                           out_min=5, out_max=60)
+    stats = {}
+    _run_and_check(reqs, num_layers=2, num_blocks=300, token_budget=1024, check_every=5,
+                   admission="prompt_preempt", stats_out=stats)
+    assert stats["num_preempted"] > 0 and stats["recomputed_tokens"] > 0
