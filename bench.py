@@ -49,6 +49,12 @@ def make_workload(name: str, decode_seqs: int = 256):
         return W.long_prompt_chunk(15), "long_prompt_32768_last_chunk_2048_bf16_H32_A128_B16"
     if name == "tiny":
         return W.tiny_fp32(), "tiny_fp32_H4_A64_B4_T6"
+    if name == "decode_gqa":
+        return (W.decode_step(num_seqs=decode_seqs, num_kv_heads=8),
+                f"decode_gqa_{decode_seqs}seq_ctx512-4096_bf16_Hq32_Hkv8_A128_B16")
+    if name == "mixed_gqa":
+        return (W.mixed_step(num_kv_heads=8),
+                "mixed_gqa_m2048_64decode_ctx256-4096_chunks661-661-662_bf16_Hq32_Hkv8_A128_B16")
     if name == "mixed_padded":
         return W.padded_equivalent(W.mixed_step()), "mixed_m2048_left_padded_to_67x662_bf16_H32_A128_B16"
     if name == "insertion":
@@ -63,16 +69,17 @@ def algorithmic_work(b):
     """Bytes and flops counted once (each KV byte read once, masked pairs not counted)."""
     e = b.elem_bytes
     H, A = b.num_heads, b.head_dim
-    kv_read = int(np.sum(b.context_lens.astype(np.int64))) * 2 * H * A * e
+    Hkv = b.kv_heads                   # keys and values have Hkv heads (grouped-query attention)
+    kv_read = int(np.sum(b.context_lens.astype(np.int64))) * 2 * Hkv * A * e
     qo = b.T * H * A * e * 2
-    append = 2 * 2 * b.T * H * A * e
+    append = 2 * 2 * b.T * Hkv * A * e
     pairs = sum(int(q) * int(p) + int(q) * (int(q) + 1) // 2 for p, q in zip(b.p, b.q_len))
     flops = 4 * A * H * pairs
     decode = b.q_len == 1
-    dec_bytes = (int(np.sum(b.context_lens[decode].astype(np.int64))) * 2 * H * A * e
+    dec_bytes = (int(np.sum(b.context_lens[decode].astype(np.int64))) * 2 * Hkv * A * e
                  + int(np.sum(decode)) * H * A * e * 2)
     pre = b.q_len > 1
-    pre_bytes = (int(np.sum(b.context_lens[pre].astype(np.int64))) * 2 * H * A * e
+    pre_bytes = (int(np.sum(b.context_lens[pre].astype(np.int64))) * 2 * Hkv * A * e
                  + int(np.sum(b.q_len[pre])) * H * A * e * 2)
     return {"bytes": kv_read + qo + append, "flops": flops, "decode_bytes": dec_bytes,
             "prefill_bytes": pre_bytes,
@@ -163,7 +170,7 @@ class Staged:
     def __init__(self, b, torch, api, W):
         dt = torch.bfloat16 if b.dtype == "bf16" else torch.float32
         self.b = b
-        self.cache = api.KVCache.empty(b.num_blocks, b.num_heads, b.block_size, b.head_dim, dt)
+        self.cache = api.KVCache.empty(b.num_blocks, b.kv_heads, b.block_size, b.head_dim, dt)
         self.cache.k.zero_()
         self.cache.v.zero_()
         sid = torch.from_numpy(b.seq_ids).cuda()
@@ -175,8 +182,8 @@ class Staged:
         rows = torch.from_numpy(np.repeat(b.seq_ids, b.q_len)).cuda()
         pos = torch.from_numpy(np.concatenate(
             [np.arange(b.p[s], b.p[s] + b.q_len[s]) for s in range(b.num_seqs)]).astype(np.int32)).cuda()
-        shape = (b.T, b.num_heads, b.head_dim)
-        self.q, self.k_new, self.v_new = (torch.empty(shape, dtype=dt, device="cuda") for _ in range(3))
+        self.q, self.k_new, self.v_new = (torch.empty((b.T, b.heads_of(kind), b.head_dim), dtype=dt, device="cuda")
+                                          for kind in (W.KIND_Q, W.KIND_K, W.KIND_V))
         for kind, t in ((W.KIND_Q, self.q), (W.KIND_K, self.k_new), (W.KIND_V, self.v_new)):
             api.cb_synth_tokens(t, b.seed, kind, b.layer, rows, pos)
         self.cu = torch.from_numpy(b.cu_seqlens_q).cuda()
@@ -184,7 +191,9 @@ class Staged:
         self.bt = torch.from_numpy(b.block_tables).cuda()
         self.slots = torch.from_numpy(b.slot_mapping).cuda()
         self.out = torch.empty_like(self.q)
-        ws = api.cb_attention_workspace_size(self.cache, b.num_seqs, b.T, b.max_context_len)
+        self.grouped = b.num_heads != b.kv_heads
+        ws = (api.cb_attention_workspace_size_gqa(self.cache, b.num_heads, b.num_seqs, b.T, b.max_context_len)
+              if self.grouped else api.cb_attention_workspace_size(self.cache, b.num_seqs, b.T, b.max_context_len))
         self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device="cuda")
         self.scale = 1.0 / math.sqrt(b.head_dim)
         self.api = api
@@ -195,12 +204,10 @@ class Staged:
 
     def attend(self, stream=None, q=None, cu=None, ctx=None, bt=None, out=None):
         b = self.b
-        self.api.cb_ragged_attention(self.q if q is None else q, self.cache,
-                                     self.cu if cu is None else cu, self.ctx if ctx is None else ctx,
-                                     self.bt if bt is None else bt, max_q_len=b.max_q_len,
-                                     max_context_len=b.max_context_len, scale=self.scale,
-                                     out=self.out if out is None else out, workspace=self.ws,
-                                     stream=stream)
+        fn = self.api.cb_ragged_attention_gqa if self.grouped else self.api.cb_ragged_attention
+        fn(self.q if q is None else q, self.cache, self.cu if cu is None else cu, self.ctx if ctx is None else ctx,
+           self.bt if bt is None else bt, max_q_len=b.max_q_len, max_context_len=b.max_context_len,
+           scale=self.scale, out=self.out if out is None else out, workspace=self.ws, stream=stream)
 
 
 # ---------------------------------------------------------------------------
@@ -210,13 +217,14 @@ class Staged:
 _RANDOM_CACHE = {}
 
 
-def _random_inputs(n_max, c_max, H, A):
-    key = (n_max, c_max, H, A)
+def _random_inputs(n_max, c_max, H, A, Hkv=None):
+    Hkv = H if Hkv is None else Hkv
+    key = (n_max, c_max, H, A, Hkv)
     if key not in _RANDOM_CACHE:
         rng = np.random.default_rng(0)
         _RANDOM_CACHE.clear()
-        _RANDOM_CACHE[key] = (rng.standard_normal((n_max, H, A)), rng.standard_normal((c_max, H, A)),
-                              rng.standard_normal((c_max, H, A)))
+        _RANDOM_CACHE[key] = (rng.standard_normal((n_max, H, A)), rng.standard_normal((c_max, Hkv, A)),
+                              rng.standard_normal((c_max, Hkv, A)))
     return _RANDOM_CACHE[key]
 
 
@@ -228,7 +236,7 @@ def time_oracle(b, budget_s: float):
     from oracle import attention as oa
     H, A = b.num_heads, b.head_dim
     scale = 1.0 / math.sqrt(A)
-    qbuf, kbuf, vbuf = _random_inputs(b.max_q_len, b.max_context_len, H, A)
+    qbuf, kbuf, vbuf = _random_inputs(b.max_q_len, b.max_context_len, H, A, b.kv_heads)
     order = np.argsort(-b.q_len, kind="stable")          # prefill chunks first, then decodes
     done_tokens, done_seqs, spent = 0, 0, 0.0
     for s in order:
@@ -583,7 +591,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=["decode", "mixed", "long", "tiny", "trace", "trace_graph",
-                                                             "mixed_padded", "insertion", "insertion_padded"])
+                                                             "decode_gqa", "mixed_gqa", "mixed_padded", "insertion",
+                                                             "insertion_padded"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--admission", default="reserve_lifetime", choices=["reserve_lifetime", "prompt_preempt"],

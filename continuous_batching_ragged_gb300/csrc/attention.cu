@@ -57,9 +57,14 @@ namespace {
 cb_status prepare(const char* who, const void* q, const cb_kv_cache* cache, const int32_t* cu_seqlens_q,
                   const int32_t* context_lens, const int32_t* block_tables, int32_t num_seqs, int32_t num_tokens,
                   int32_t max_blocks_per_seq, int32_t max_q_len, int32_t max_context_len, float scale, void* out,
-                  const int32_t* dims, bool plan_only, cb::AttnArgs& a) {
+                  const int32_t* dims, bool plan_only, cb::AttnArgs& a, int32_t num_q_heads = 0) {
   cb_status st = check_cache(cache, who);
   if (st != CB_OK) return st;
+  if (num_q_heads == 0) num_q_heads = cache->num_heads;
+  if (num_q_heads < 1 || num_q_heads % cache->num_heads != 0)
+    return cb::fail(CB_ERR_INVALID, "%s: num_q_heads must be a positive multiple of the cache's heads", who);
+  if (num_q_heads != cache->num_heads && (cache->dtype != CB_DTYPE_BF16 || cache->block_size % 16 != 0))
+    return cb::fail(CB_ERR_UNSUPPORTED, "%s: grouped KV heads need bf16 and a block size multiple of 16", who);
   if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq < 0 || max_q_len < 0 || max_context_len < 0)
     return cb::fail(CB_ERR_INVALID, "%s: negative size", who);
   if (num_seqs == 0 || num_tokens == 0) {
@@ -95,7 +100,8 @@ cb_status prepare(const char* who, const void* q, const cb_kv_cache* cache, cons
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.num_blocks = cache->num_blocks;
   a.block_size = cache->block_size;
-  a.num_heads = cache->num_heads;
+  a.num_heads = num_q_heads;
+  a.num_kv_heads = cache->num_heads;
   a.head_dim = cache->head_dim;
   a.max_q_len = max_q_len;
   a.max_context_len = max_context_len;
@@ -140,6 +146,36 @@ std::unordered_map<const void*, PlanRecord> g_plans;
 
 }  // namespace
 
+namespace {
+
+cb_status attention(const char* who, const void* q, int32_t num_q_heads, const cb_kv_cache* cache,
+                    const int32_t* cu_seqlens_q, const int32_t* context_lens, const int32_t* block_tables,
+                    int32_t num_seqs, int32_t num_tokens, int32_t max_blocks_per_seq, int32_t max_q_len,
+                    int32_t max_context_len, float scale, void* out, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  cb::AttnArgs a;
+  cb_status st = prepare(who, q, cache, cu_seqlens_q, context_lens, block_tables, num_seqs, num_tokens,
+                         max_blocks_per_seq, max_q_len, max_context_len, scale, out, nullptr, false, a, num_q_heads);
+  if (st != CB_OK || num_seqs == 0) return st;
+  cudaStream_t main = static_cast<cudaStream_t>(stream);
+  if (cache->dtype == CB_DTYPE_F32) return cb::launch_split_kv(a, true, workspace, workspace_bytes, main);
+
+  // bf16: the step plan first, then the persistent kernels over its work lists
+  cb::StepPlan plan;
+  st = cb::step_plan_layout(workspace, workspace_bytes, num_seqs, num_tokens, a.num_heads, cache->head_dim,
+                            max_context_len, &plan);
+  if (st != CB_OK) return st;
+  plan.dec_ctas = cb::decode_persistent_ctas(a);
+  plan.dec_groups = a.num_heads / cb::decode_group_heads(a);
+  st = cb::launch_plan(a, plan, main);
+  if (st != CB_OK) return st;
+  if (max_q_len == 1) return cb::launch_decode_persistent(a, plan, true, main);
+  if (max_q_len == num_tokens && num_seqs == 1) return cb::launch_prefill_tc(a, plan, true, main);
+  return run_both(a, plan, main);
+}
+
+}  // namespace
+
 extern "C" cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache,
                                          const int32_t* cu_seqlens_q, const int32_t* context_lens,
                                          const int32_t* block_tables, int32_t num_seqs,
@@ -147,25 +183,31 @@ extern "C" cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache
                                          int32_t max_q_len, int32_t max_context_len, float scale,
                                          void* out, void* workspace, size_t workspace_bytes,
                                          void* stream) {
-  cb::AttnArgs a;
-  cb_status st = prepare("cb_ragged_attention", q, cache, cu_seqlens_q, context_lens, block_tables, num_seqs,
-                         num_tokens, max_blocks_per_seq, max_q_len, max_context_len, scale, out, nullptr, false,
-                         a);
-  if (st != CB_OK || num_seqs == 0) return st;
-  cudaStream_t main = static_cast<cudaStream_t>(stream);
-  if (cache->dtype == CB_DTYPE_F32) return cb::launch_split_kv(a, true, workspace, workspace_bytes, main);
+  return attention("cb_ragged_attention", q, 0, cache, cu_seqlens_q, context_lens, block_tables, num_seqs,
+                   num_tokens, max_blocks_per_seq, max_q_len, max_context_len, scale, out, workspace,
+                   workspace_bytes, stream);
+}
 
-  // bf16: the step plan first, then the persistent kernels over its work lists
-  cb::StepPlan plan;
-  st = cb::step_plan_layout(workspace, workspace_bytes, num_seqs, num_tokens, cache->num_heads,
-                            cache->head_dim, max_context_len, &plan);
-  if (st != CB_OK) return st;
-  plan.dec_ctas = cb::decode_persistent_ctas();
-  st = cb::launch_plan(a, plan, main);
-  if (st != CB_OK) return st;
-  if (max_q_len == 1) return cb::launch_decode_persistent(a, plan, true, main);
-  if (max_q_len == num_tokens && num_seqs == 1) return cb::launch_prefill_tc(a, plan, true, main);
-  return run_both(a, plan, main);
+extern "C" size_t cb_attention_workspace_size_gqa(const cb_kv_cache* cache, int32_t num_q_heads,
+                                                  int32_t num_seqs, int32_t num_tokens,
+                                                  int32_t max_context_len) {
+  if (!cache || num_q_heads < 1 || num_seqs < 0 || num_tokens < 0 || max_context_len < 0) return 0;
+  const bool row_mode = cache->dtype == CB_DTYPE_F32;
+  return cb::split_kv_workspace_bytes(row_mode, num_seqs, num_tokens, num_q_heads, cache->head_dim,
+                                      max_context_len);
+}
+
+extern "C" cb_status cb_ragged_attention_gqa(const void* q, int32_t num_q_heads, const cb_kv_cache* cache,
+                                             const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                             const int32_t* block_tables, int32_t num_seqs,
+                                             int32_t num_tokens, int32_t max_blocks_per_seq,
+                                             int32_t max_q_len, int32_t max_context_len, float scale,
+                                             void* out, void* workspace, size_t workspace_bytes,
+                                             void* stream) {
+  if (num_q_heads < 1) return cb::fail(CB_ERR_INVALID, "cb_ragged_attention_gqa: num_q_heads < 1");
+  return attention("cb_ragged_attention_gqa", q, num_q_heads, cache, cu_seqlens_q, context_lens, block_tables,
+                   num_seqs, num_tokens, max_blocks_per_seq, max_q_len, max_context_len, scale, out, workspace,
+                   workspace_bytes, stream);
 }
 
 extern "C" cb_status cb_plan_step(const cb_kv_cache* cache, const int32_t* cu_seqlens_q,
@@ -187,7 +229,8 @@ extern "C" cb_status cb_plan_step(const cb_kv_cache* cache, const int32_t* cu_se
   st = cb::step_plan_layout(workspace, workspace_bytes, num_seqs, num_tokens, cache->num_heads, cache->head_dim,
                             max_context_len, &rec.plan);
   if (st != CB_OK) return st;
-  rec.plan.dec_ctas = cb::decode_persistent_ctas();
+  rec.plan.dec_ctas = cb::decode_persistent_ctas(a);
+  rec.plan.dec_groups = a.num_heads / cb::decode_group_heads(a);
   st = cb::launch_plan(a, rec.plan, static_cast<cudaStream_t>(stream));
   if (st != CB_OK) return st;
   rec.cu = cu_seqlens_q;

@@ -98,6 +98,7 @@ extern "C" cb_status cb_decode_attention_noalloc(const void* q, const cb_kv_cach
   a.num_blocks = cache->num_blocks;
   a.block_size = cache->block_size;
   a.num_heads = cache->num_heads;
+  a.num_kv_heads = cache->num_heads;
   a.head_dim = cache->head_dim;
   a.max_q_len = 1;
   a.max_context_len = max_context_len;

@@ -22,7 +22,8 @@ struct AttnArgs {
   int32_t max_blocks_per_seq;
   int32_t num_blocks;
   int32_t block_size;
-  int32_t num_heads;
+  int32_t num_heads;      // query heads (q and out rows)
+  int32_t num_kv_heads;   // heads of the cache pools; num_heads is a multiple of it
   int32_t head_dim;
   int32_t max_q_len;
   int32_t max_context_len;
@@ -63,6 +64,7 @@ struct StepPlan {
   int32_t pre_cap;        // capacity of pre_seqs and pre_scratch (pre_units holds pre_cap * H)
   uint32_t tag;           // this call's tag: the plan writes it to header[4], the kernels check it
   int32_t dec_ctas;       // CTAs of the persistent decode grid (sets the split length)
+  int32_t dec_groups;     // decode units per decode item (query-head groups)
 };
 
 // Workspace of a bf16 step (plan + split scratch) and its carving.
@@ -77,8 +79,10 @@ cb_status step_plan_layout(void* workspace, size_t workspace_bytes, int32_t num_
 // launch_after_plan may start while it runs and wait for it on the device.
 cb_status launch_plan(const AttnArgs& a, const StepPlan& plan, cudaStream_t stream);
 
-// CTAs of the persistent decode grid on the current device (0 on error).
-int decode_persistent_ctas();
+// CTAs of the persistent decode grid on the current device (0 on error), and
+// the query heads each of its units covers.
+int decode_persistent_ctas(const AttnArgs& a);
+int decode_group_heads(const AttnArgs& a);
 
 // Persistent decode over the plan's decode items (bf16, head_dim 128, block
 // size a multiple of 16).  `after_plan`: launched right behind launch_plan on

@@ -171,9 +171,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
   block_excl_scan(dec_keys, warp_sums, total_keys);
   // Keys per decode split: every split pays a fixed cost (its merge and a
   // partial result round trip), so splits are as long as possible while the
-  // decode grid still gets kUnitsPerCta units per CTA to balance over.
+  // decode grid still gets kUnitsPerCta units per CTA to balance over (a
+  // decode item is dec_groups units, one per group of query heads).
   const uint64_t target = uint64_t(p.dec_ctas > 0 ? p.dec_ctas : 1) * kUnitsPerCta;
-  const uint64_t want = (total_keys * uint64_t(a.num_heads) + target - 1) / target;
+  const uint64_t groups = uint64_t(p.dec_groups > 0 ? p.dec_groups : a.num_heads);
+  const uint64_t want = (total_keys * groups + target - 1) / target;
   const uint64_t per = want < uint64_t(kSplitKeys) ? uint64_t(kSplitKeys) : want;
   const uint64_t rounded = (per + kSplitKeys - 1) / kSplitKeys * kSplitKeys;
   const int split = rounded > (uint64_t(1) << 30) ? (1 << 30) : int(rounded);
@@ -318,6 +320,7 @@ cb_status step_plan_layout(void* workspace, size_t workspace_bytes, int32_t num_
   plan->dec_cap = int32_t(S * splits);
   plan->pre_cap = int32_t(pre_cap);
   plan->dec_ctas = 0;
+  plan->dec_groups = 0;
   static std::atomic<uint32_t> next_tag{1};
   plan->tag = next_tag.fetch_add(1);
   return CB_OK;

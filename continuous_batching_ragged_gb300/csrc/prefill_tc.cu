@@ -143,15 +143,15 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t x, 
 // load, stores its box index (or `oob`, zero fill) in the ring slot of tile j,
 // and asks TMA to prefetch that box into L2 for the load a few tiles later.
 __device__ __forceinline__ void stage_boxes(int j, int B, int ctx, const int32_t* bt, const AttnArgs& a,
-                                            int h, int lane, int* ring, const CUtensorMap* tm) {
+                                            int hkv, int lane, int* ring, const CUtensorMap* tm) {
   const int bpt = BN / B;
   if (lane < bpt) {
     const int lb = j * bpt + lane;
-    int z = a.num_blocks * a.num_heads;
+    int z = a.num_blocks * a.num_kv_heads;
     if (lb * B < ctx) {
       const int blk = bt[lb];
       if (blk >= 0 && blk < a.num_blocks) {
-        z = blk * a.num_heads + h;
+        z = blk * a.num_kv_heads + hkv;
         tma_prefetch_l2_3d(tm, 0, 0, z);
         tma_prefetch_l2_3d(tm, 64, 0, z);
       } else {
@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int B = a.block_size;
-  const int H = a.num_heads;
+  const int H = a.num_heads;                       // query heads
+  const int G = H / a.num_kv_heads;                // query heads per K/V head (grouped-query attention)
 
   grid_dependency_wait();                          // the plan kernel has finished
   const uint32_t seen_tag = uint32_t(__ldcg(w.header + 4));
@@ -343,14 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       const int q_at = min(kKStages - 1, sh.n_tiles);   // K tiles requested before the Q load
       for (int j = 0; j < min(kLookAhead, sh.n_tiles); ++j)
-        stage_boxes(j, B, it.ctx, bt, a, it.h, lane, ring, &tm_k);
+        stage_boxes(j, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_k);
       for (int j = 0; j < sh.n_tiles; ++j) {
         if (j == q_at && !load_q()) {
           ok = false;
           site = kSitePfQFree;
           break;
         }
-        if (j + kLookAhead < sh.n_tiles) stage_boxes(j + kLookAhead, B, it.ctx, bt, a, it.h, lane, ring, &tm_k);
+        if (j + kLookAhead < sh.n_tiles) stage_boxes(j + kLookAhead, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_k);
         const uint32_t g = kc + j;
         const int st = g % kKStages;
         if (g >= kKStages && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_KE + st), ((g / kKStages) - 1) & 1))) {
@@ -398,9 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const UnitShape sh = unit_shape(it);
       const int32_t* bt = a.block_tables + size_t(it.s) * a.max_blocks_per_seq;
       for (int j = 0; j < min(kLookAhead, sh.n_tiles); ++j)
-        stage_boxes(j, B, it.ctx, bt, a, it.h, lane, ring, &tm_v);
+        stage_boxes(j, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_v);
       for (int j = 0; j < sh.n_tiles; ++j) {
-        if (j + kLookAhead < sh.n_tiles) stage_boxes(j + kLookAhead, B, it.ctx, bt, a, it.h, lane, ring, &tm_v);
+        if (j + kLookAhead < sh.n_tiles) stage_boxes(j + kLookAhead, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_v);
         const uint32_t g = vc + j;
         const int st = g % kVStages;
         if (g >= kVStages && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_VE + st), ((g / kVStages) - 1) & 1))) {
@@ -687,8 +688,8 @@ cb_status launch_prefill_tc(const AttnArgs& a, const StepPlan& plan, bool after_
   const int B = a.block_size;
   if (B < 8 || B > BN || (B & (B - 1)) != 0)
     return fail(CB_ERR_UNSUPPORTED, "prefill chunks: block_size must be a power of two in [8, 128]");
-  if (int64_t(a.num_blocks) * a.num_heads >= (int64_t(1) << 31))
-    return fail(CB_ERR_UNSUPPORTED, "prefill chunks: num_blocks * num_heads must fit in int32");
+  if (int64_t(a.num_blocks) * a.num_kv_heads >= (int64_t(1) << 31))
+    return fail(CB_ERR_UNSUPPORTED, "prefill chunks: num_blocks * num_kv_heads must fit in int32");
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return CB_ERR_CUDA;
   CUtensorMap tq, tk, tv;
@@ -703,7 +704,7 @@ cb_status launch_prefill_tc(const AttnArgs& a, const StepPlan& plan, bool after_
     if (r != CUDA_SUCCESS) return fail(CB_ERR_CUDA, "encoding the Q tensor map failed (%d)", int(r));
   }
   {
-    const cuuint64_t dims[3] = {cuuint64_t(HD), cuuint64_t(B), cuuint64_t(a.num_blocks) * a.num_heads};
+    const cuuint64_t dims[3] = {cuuint64_t(HD), cuuint64_t(B), cuuint64_t(a.num_blocks) * a.num_kv_heads};
     const cuuint64_t strides[2] = {cuuint64_t(HD) * 2, cuuint64_t(B) * HD * 2};
     const cuuint32_t box[3] = {64, cuuint32_t(B), 1};
     CUresult r = enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k_pool), dims, strides,

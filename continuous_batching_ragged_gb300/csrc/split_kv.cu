@@ -49,6 +49,7 @@ struct SplitArgs {
   int32_t* claims;          // persistent decode: claim counter
   int32_t item_cap;         // persistent decode: capacity of the item list
   uint32_t tag;             // persistent decode: the plan's call tag
+  int32_t n_groups;         // persistent decode: units per item (query-head groups)
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -331,24 +332,123 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_kernel(const SplitArgs s
   finish_split<T, A, ROW_MODE, EPV, LPR>(sa, pl, split, h, m_run, l_run, acc, sm);
 }
 
-// One decode unit: (sequence, split, head) and the keys [k0, k1) it covers.
+// One decode unit: (sequence, split, group of GU query heads sharing one KV
+// head) and the keys [k0, k1) it covers.
 struct Unit {
   int u;                      // claimed unit index; >= the unit count: no more work
-  int s, t, h, split, nsplit, k0, k1;
+  int s, t, grp, h0, hkv, split, nsplit, k0, k1;
 };
+
+// Shared scratch of the epilogue of a unit of GU query heads.
+template <int GU>
+struct GroupSmem {
+  float acc[GU][kWarps][128];
+  float m[GU][kWarps], l[GU][kWarps];
+  int last;
+};
+
+// Combine the warps' (m, l, acc) of each of the unit's GU heads, then either
+// write the output rows (one split) or publish the partials and, in the last
+// CTA of the (sequence, group) to finish, merge every split by log-sum-exp.
+template <int GU>
+__device__ __forceinline__ void finish_group(const SplitArgs& sa, const Unit& U, const float (&m_run)[GU],
+                                             const float (&l_run)[GU], float (&acc)[GU][8], GroupSmem<GU>& sm) {
+  using T = __nv_bfloat16;
+  constexpr int A = 128, EPV = 8, LPR = 16;
+  const AttnArgs& a = sa.a;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane / LPR, c = lane % LPR;
+#pragma unroll
+  for (int hh = 0; hh < GU; ++hh) {
+    // lanes of the two row groups hold the same chunk: add them
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[hh][e] += __shfl_xor_sync(0xffffffffu, acc[hh][e], LPR);
+    if (g == 0) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) sm.acc[hh][warp][c * EPV + e] = acc[hh][e];
+    }
+    if (lane == 0) {
+      sm.m[hh][warp] = m_run[hh];
+      sm.l[hh][warp] = l_run[hh];
+    }
+  }
+  __syncthreads();
+  const int d = threadIdx.x;                // one output dimension per thread (128 threads)
+  const int H = a.num_heads;
+  float* part0 = sa.partials + (size_t(U.s) * H * sa.max_splits) * (A + 2);
+#pragma unroll
+  for (int hh = 0; hh < GU; ++hh) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.m[hh][w]);
+    float L = 0.f, o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = ex2(sm.m[hh][w] - M);   // a warp with no keys has m = -inf: weight 0
+      L = fmaf(sm.l[hh][w], f, L);
+      o = fmaf(sm.acc[hh][w][d], f, o);
+    }
+    const int h = U.h0 + hh;
+    if (U.nsplit == 1) {
+      store1(static_cast<T*>(a.out) + (size_t(U.t) * H + h) * A + d, o / L);
+    } else {
+      float* part = part0 + (size_t(h) * sa.max_splits + U.split) * (A + 2);
+      part[d] = o;
+      if (d == 0) {
+        part[A] = M;
+        part[A + 1] = L;
+      }
+    }
+  }
+  if (U.nsplit == 1) return;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t* ticket = sa.tickets + size_t(U.s) * sa.n_groups + U.grp;
+    sm.last = atomicAdd(ticket, 1) == U.nsplit - 1;
+    if (sm.last) *ticket = 0;             // every split has arrived: reset for the next call
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();
+#pragma unroll
+  for (int hh = 0; hh < GU; ++hh) {
+    const int h = U.h0 + hh;
+    const float* part = part0 + size_t(h) * sa.max_splits * (A + 2);
+    float MM = -INFINITY;
+    for (int k = 0; k < U.nsplit; ++k) MM = fmaxf(MM, __ldcg(part + size_t(k) * (A + 2) + A));
+    float LL = 0.f, oo = 0.f;
+    for (int k = 0; k < U.nsplit; ++k) {
+      const float* pk = part + size_t(k) * (A + 2);
+      const float f = ex2(__ldcg(pk + A) - MM);
+      LL = fmaf(__ldcg(pk + A + 1), f, LL);
+      oo = fmaf(__ldcg(pk + d), f, oo);
+    }
+    store1(static_cast<T*>(a.out) + (size_t(U.t) * H + h) * A + d, oo / LL);
+  }
+}
 
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+template <int GU>
+constexpr uint32_t bulk_smem_bytes() {
+  return kWarps * kStages * 2 * kTileBytes + kWarps * kStages * (8 + 4) + sizeof(GroupSmem<GU>) + 2 * sizeof(Unit);
+}
+
 // Decode rows, bf16, head_dim 128, block size a multiple of 16, persistent:
-// a fixed grid of CTAs claims units (sequence, split, head) from the step
+// a fixed grid of CTAs claims units (sequence, split, group of GU query heads
+// that share one KV head -- GU = 1 for multi-head attention) from the step
 // plan until none are left.  Each warp streams its 16-key K/V tiles (4 KB
 // each, contiguous in the pool) with bulk async copies into a private
-// kStages-deep shared ring.  The ring runs across units: once a warp has
-// issued the last tile of its current unit it goes on with the first tiles of
-// the unit the CTA claimed next, so the copies of the next unit are in flight
-// while the current one is merged and written.
+// kStages-deep shared ring, and every tile serves all GU heads of the unit.
+// The ring runs across units: once a warp has issued the last tile of its
+// current unit it goes on with the first tiles of the unit the CTA claimed
+// next, so the copies of the next unit are in flight while the current one
+// is merged and written.
+template <int GU>
 __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const SplitArgs sa) {
   using T = __nv_bfloat16;
   constexpr int A = 128, EPV = 8, LPR = 16, RPL = 2, NR = 8;
@@ -361,9 +461,9 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * 2 * kTileBytes) + warp * kStages;
   int* valid = reinterpret_cast<int*>(smem + kWarps * kStages * 2 * kTileBytes + kWarps * kStages * 8) +
                warp * kStages;
-  MergeSmem<A>& sm = *reinterpret_cast<MergeSmem<A>*>(smem + kWarps * kStages * 2 * kTileBytes +
-                                                      kWarps * kStages * 8 + kWarps * kStages * 4);
-  Unit* slots = reinterpret_cast<Unit*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(MergeSmem<A>));   // [2]
+  GroupSmem<GU>& sm = *reinterpret_cast<GroupSmem<GU>*>(smem + kWarps * kStages * 2 * kTileBytes +
+                                                        kWarps * kStages * 8 + kWarps * kStages * 4);
+  Unit* slots = reinterpret_cast<Unit*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(GroupSmem<GU>));   // [2]
   __shared__ int abort_flag;
   if (lane == 0) {
     for (int st = 0; st < kStages; ++st) sm100::mbar_init(sm100::smem_u32(&bars[st]), 1);
@@ -371,28 +471,32 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const 
   }
   if (threadIdx.x == 0) abort_flag = 0;
   grid_dependency_wait();                   // the plan kernel has finished
-  const int H = a.num_heads;
+  const int H = a.num_heads;                // query heads
+  const int G = H / a.num_kv_heads;         // query heads per KV head
+  const int n_groups = sa.n_groups;         // = H / GU
   const uint32_t seen_tag = uint32_t(__ldcg(sa.header + 4));
   const int n_items = __ldcg(sa.header);
   if (seen_tag != sa.tag || n_items < 0 || n_items > sa.item_cap || __ldcg(sa.header + 5) < kSplitKeys) {
     if (threadIdx.x == 0) raise_error(a.err, kErrInvalid);
     return;
   }
-  const int n_units = n_items * H;
+  const int n_units = n_items * n_groups;
   if (int(blockIdx.x) >= n_units) return;   // no unit could be left for this CTA
   const int split_keys = __ldcg(sa.header + 5);            // keys per split, chosen by the plan
   const T* kp = static_cast<const T*>(a.k_pool);
   const T* vp = static_cast<const T*>(a.v_pool);
   const int B = a.block_size;
-  const size_t blk_stride = size_t(H) * B * A;
+  const size_t blk_stride = size_t(a.num_kv_heads) * B * A;
 
   // one thread: claim the next unit and describe it in `slot`
   auto claim = [&](Unit& slot) {
     Unit U;
     U.u = abort_flag ? n_units : atomicAdd(sa.claims, 1);
     if (U.u < n_units) {
-      const int2 it = __ldcg(sa.items + U.u / H);
-      U.h = U.u % H;
+      const int2 it = __ldcg(sa.items + U.u / n_groups);
+      U.grp = U.u % n_groups;
+      U.h0 = U.grp * GU;
+      U.hkv = U.h0 / G;
       U.s = it.x;
       U.split = it.y;
       bool bad = U.s < 0 || U.s >= a.num_seqs || U.split < 0;
@@ -413,8 +517,11 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const 
     }
     slot = U;
   };
-  auto load_q_raw = [&](const Unit& U) -> uint4 {
-    return *reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + (size_t(U.t) * H + U.h) * A + c * EPV);
+  auto load_q_raw = [&](const Unit& U, uint4 (&q)[GU]) {
+#pragma unroll
+    for (int hh = 0; hh < GU; ++hh)
+      q[hh] = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + (size_t(U.t) * H + U.h0 + hh) * A +
+                                              c * EPV);
   };
   // tiles of unit U that this warp takes (tiles warp, warp + kWarps, ...)
   auto warp_tiles = [&](const Unit& U) -> int {
@@ -432,7 +539,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const 
       const int blk = a.block_tables[size_t(U.s) * a.max_blocks_per_seq + j0 / B];
       if (blk >= 0 && blk < a.num_blocks) {
         valid[st] = 1;
-        const size_t off = size_t(blk) * blk_stride + size_t(U.h) * B * A + size_t(j0 % B) * A;
+        const size_t off = size_t(blk) * blk_stride + size_t(U.hkv) * B * A + size_t(j0 % B) * A;
         const uint32_t dst = sm100::smem_u32(ring + st * 2 * kTileBytes);
         sm100::mbar_arrive_expect_tx(bar, 2 * kTileBytes);
         sm100::bulk_load(dst, kp + off, kTileBytes, bar);
@@ -457,8 +564,10 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const 
   __syncthreads();
   Unit U0 = slots[0];
   int n0 = warp_tiles(U0), i0 = 0;          // tiles of U0: count, issued so far
-  uint4 q_raw = make_uint4(0, 0, 0, 0);     // this lane's 16 bytes of U0's query row
-  if (U0.u < n_units) q_raw = load_q_raw(U0);
+  uint4 q_raw[GU];                          // this lane's 16 bytes of U0's query rows
+#pragma unroll
+  for (int hh = 0; hh < GU; ++hh) q_raw[hh] = make_uint4(0, 0, 0, 0);
+  if (U0.u < n_units) load_q_raw(U0, q_raw);
   for (int k = 0; U0.u < n_units; ++k) {
     __syncthreads();                        // slot (k + 1) % 2 written; slot k % 2 read by every thread
     const Unit U1 = slots[(k + 1) & 1];
@@ -476,15 +585,23 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const 
       }
     };
     top_up();
-    float qf[EPV];
-    Vec16<T>::to_float(q_raw, qf);
+    float qf[GU][EPV];
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) qf[e] *= a.scale_log2;    // scores in the exp2 domain
-    if (U1.u < n_units) q_raw = load_q_raw(U1);             // in flight while U0 streams
-    float m_run = -INFINITY, l_run = 0.f;
-    float acc[EPV];
+    for (int hh = 0; hh < GU; ++hh) {
+      Vec16<T>::to_float(q_raw[hh], qf[hh]);
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
+      for (int e = 0; e < EPV; ++e) qf[hh][e] *= a.scale_log2;    // scores in the exp2 domain
+    }
+    if (U1.u < n_units) load_q_raw(U1, q_raw);                   // in flight while U0 streams
+    float m_run[GU], l_run[GU];
+    float acc[GU][EPV];
+#pragma unroll
+    for (int hh = 0; hh < GU; ++hh) {
+      m_run[hh] = -INFINITY;
+      l_run[hh] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) acc[hh][e] = 0.f;
+    }
     for (int it = 0; it < n0; ++it) {
       const int st = consumed % kStages;
       if (!__all_sync(0xffffffffu, sm100::mbar_wait(sm100::smem_u32(&bars[st]), (consumed / kStages) & 1))) {
@@ -505,18 +622,14 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const 
         kv[i] = in ? *reinterpret_cast<const uint4*>(kt + r * 256 + c * 16) : make_uint4(0, 0, 0, 0);
         vv[i] = in ? *reinterpret_cast<const uint4*>(kt + kTileBytes + r * 256 + c * 16) : make_uint4(0, 0, 0, 0);
       }
-      tile_update<T, EPV, LPR, RPL, NR>(qf, kv, vv, base, U0.k1, lane, m_run, l_run, acc);
+#pragma unroll
+      for (int hh = 0; hh < GU; ++hh)
+        tile_update<T, EPV, LPR, RPL, NR>(qf[hh], kv, vv, base, U0.k1, lane, m_run[hh], l_run[hh], acc[hh]);
       __syncwarp();                         // every lane has used what it read: the slot may be refilled
       ++consumed;
       top_up();
     }
-    RowPlan pl;
-    pl.s = U0.s;
-    pl.t = U0.t;
-    pl.nsplit = U0.nsplit;
-    pl.k0 = U0.k0;
-    pl.k1 = U0.k1;
-    finish_split<T, A, false, EPV, LPR>(sa, pl, U0.split, U0.h, m_run, l_run, acc, sm);
+    finish_group<GU>(sa, U0, m_run, l_run, acc, sm);
     U0 = U1;
     n0 = n1;
     i0 = i1;
@@ -528,11 +641,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const 
   }
 }
 
-constexpr uint32_t kBulkSmem = kWarps * kStages * 2 * kTileBytes + kWarps * kStages * (8 + 4) +
-                               sizeof(MergeSmem<128>) + 2 * sizeof(Unit);
-
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-bool g_bulk_attr[64] = {};
 
 }  // namespace
 
@@ -551,27 +660,47 @@ static void launch(const SplitArgs& sa, dim3 grid, cudaStream_t stream) {
   split_kv_kernel<T, A, ROW><<<grid, kWarps * 32, 0, stream>>>(sa);
 }
 
-int decode_persistent_ctas() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    fail(CB_ERR_UNSUPPORTED, "decode: no usable current device");
-    return 0;
-  }
+// Query heads per decode unit: the largest of 4, 3, 2, 1 dividing the query
+// heads per KV head (1 for multi-head attention).
+int decode_group_heads(const AttnArgs& a) {
+  const int G = a.num_kv_heads > 0 ? a.num_heads / a.num_kv_heads : 1;
+  for (int gu = 4; gu > 1; --gu)
+    if (G % gu == 0) return gu;
+  return 1;
+}
+
+template <int GU>
+static int persistent_ctas(int dev) {
   static int ctas_per_sm[64] = {};
-  if (!g_bulk_attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(split_kv_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kBulkSmem));
+  static bool ready[64] = {};
+  if (!ready[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(split_kv_persistent_kernel<GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(bulk_smem_bytes<GU>()));
     if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas_per_sm[dev], split_kv_persistent_kernel,
-                                                        kWarps * 32, kBulkSmem);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas_per_sm[dev], split_kv_persistent_kernel<GU>,
+                                                        kWarps * 32, bulk_smem_bytes<GU>());
     if (e != cudaSuccess) {
       cuda_fail(e, "split-KV: kernel attributes");
       return 0;
     }
     if (ctas_per_sm[dev] < 1) ctas_per_sm[dev] = 1;
-    g_bulk_attr[dev] = true;
+    ready[dev] = true;
   }
   return ctas_per_sm[dev] * sm_count();
+}
+
+int decode_persistent_ctas(const AttnArgs& a) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    fail(CB_ERR_UNSUPPORTED, "decode: no usable current device");
+    return 0;
+  }
+  switch (decode_group_heads(a)) {
+    case 4: return persistent_ctas<4>(dev);
+    case 3: return persistent_ctas<3>(dev);
+    case 2: return persistent_ctas<2>(dev);
+    default: return persistent_ctas<1>(dev);
+  }
 }
 
 static bool persistent_ok(const AttnArgs& a) {
@@ -592,6 +721,8 @@ cb_status launch_decode_persistent(const AttnArgs& a, const StepPlan& plan, bool
   sa.tag = plan.tag;
   if (!persistent_ok(a)) {
     // other shapes: one CTA per (split, head, sequence); the plan has cleared the tickets
+    if (a.num_kv_heads != a.num_heads)
+      return fail(CB_ERR_UNSUPPORTED, "split-KV path: grouped KV heads need bf16, head_dim 128, block size % 16 == 0");
     if (a.num_seqs > 65535) return fail(CB_ERR_UNSUPPORTED, "split-KV path: more than 65535 rows");
     const dim3 grid(unsigned(sa.max_splits), unsigned(a.num_heads), unsigned(a.num_seqs));
     const bool bf16 = a.dtype == CB_DTYPE_BF16;
@@ -603,14 +734,32 @@ cb_status launch_decode_persistent(const AttnArgs& a, const StepPlan& plan, bool
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? CB_OK : cuda_fail(e, "split-KV launch");
   }
-  const int ctas = decode_persistent_ctas();
+  const int gu = decode_group_heads(a);
+  sa.n_groups = a.num_heads / gu;
+  const int ctas = decode_persistent_ctas(a);
   if (ctas < 1) return CB_ERR_CUDA;
   // never more CTAs than units could exist
-  const int64_t max_units = int64_t(a.num_seqs) * plan.max_splits * a.num_heads;
+  const int64_t max_units = int64_t(a.num_seqs) * plan.max_splits * sa.n_groups;
   const int64_t grid = std::min<int64_t>(ctas, max_units);
   if (grid < 1) return CB_OK;
-  cudaError_t e = launch_kernel(split_kv_persistent_kernel, dim3(unsigned(grid)), dim3(kWarps * 32), kBulkSmem,
-                                stream, after_plan, sa);
+  cudaError_t e;
+  switch (gu) {
+    case 4:
+      e = launch_kernel(split_kv_persistent_kernel<4>, dim3(unsigned(grid)), dim3(kWarps * 32), bulk_smem_bytes<4>(),
+                        stream, after_plan, sa);
+      break;
+    case 3:
+      e = launch_kernel(split_kv_persistent_kernel<3>, dim3(unsigned(grid)), dim3(kWarps * 32), bulk_smem_bytes<3>(),
+                        stream, after_plan, sa);
+      break;
+    case 2:
+      e = launch_kernel(split_kv_persistent_kernel<2>, dim3(unsigned(grid)), dim3(kWarps * 32), bulk_smem_bytes<2>(),
+                        stream, after_plan, sa);
+      break;
+    default:
+      e = launch_kernel(split_kv_persistent_kernel<1>, dim3(unsigned(grid)), dim3(kWarps * 32), bulk_smem_bytes<1>(),
+                        stream, after_plan, sa);
+  }
   return e == cudaSuccess ? CB_OK : cuda_fail(e, "split-KV: persistent launch");
 }
 
@@ -624,7 +773,8 @@ cb_status launch_split_kv(const AttnArgs& a, bool row_mode, void* workspace,
     cb_status st = step_plan_layout(workspace, workspace_bytes, a.num_seqs, a.num_tokens, a.num_heads,
                                     a.head_dim, a.max_context_len, &plan);
     if (st != CB_OK) return st;
-    plan.dec_ctas = decode_persistent_ctas();
+    plan.dec_ctas = decode_persistent_ctas(a);
+    plan.dec_groups = a.num_heads / decode_group_heads(a);
     st = launch_plan(a, plan, stream);
     if (st != CB_OK) return st;
     return launch_decode_persistent(a, plan, true, stream);

@@ -143,6 +143,14 @@ class RaggedBatch:
     num_blocks: int                 # pool size in blocks
     name: str = ""
     useful_tokens: Optional[int] = None   # of a padded batch: the real query tokens
+    num_kv_heads: Optional[int] = None    # key/value heads (grouped-query attention); None = num_heads
+
+    @property
+    def kv_heads(self) -> int:
+        return self.num_kv_heads if self.num_kv_heads else self.num_heads
+
+    def heads_of(self, kind: int) -> int:
+        return self.num_heads if kind == KIND_Q else self.kv_heads
 
     @property
     def num_seqs(self) -> int:
@@ -190,10 +198,12 @@ class RaggedBatch:
 
     # -- values ------------------------------------------------------------
     def packed(self, kind: int) -> np.ndarray:
-        """This step's tokens of ``kind`` packed as [T, H, A] (fp32 holding dtype values)."""
-        out = np.empty((self.T, self.num_heads, self.head_dim), dtype=np.float32)
+        """This step's tokens of ``kind`` packed as [T, heads, A] (fp32 holding dtype
+        values); queries have num_heads heads, keys and values kv_heads."""
+        nh = self.heads_of(kind)
+        out = np.empty((self.T, nh, self.head_dim), dtype=np.float32)
         cu = self.cu_seqlens_q
-        heads = range(self.num_heads)
+        heads = range(nh)
         for s in range(self.num_seqs):
             pos = np.arange(self.p[s], self.p[s] + self.q_len[s])
             out[cu[s]:cu[s + 1]] = token_values(self.seed, kind, self.layer, int(self.seq_ids[s]),
@@ -204,7 +214,7 @@ class RaggedBatch:
                 upto: Optional[int] = None) -> np.ndarray:
         """Sequence s's keys or values for positions [0, upto) (default: context_len)."""
         if heads is None:
-            heads = range(self.num_heads)
+            heads = range(self.heads_of(kind))
         n = int(self.context_lens[s]) if upto is None else int(upto)
         return token_values(self.seed, kind, self.layer, int(self.seq_ids[s]),
                             np.arange(n), heads, self.head_dim, self.dtype)
@@ -213,7 +223,7 @@ class RaggedBatch:
         """Host pool [num_blocks, H, B, A] holding every sequence's cached prefix
         (positions < p) at its block-table slots; every other slot holds ``sentinel``."""
         B = self.block_size
-        pool = np.full((self.num_blocks, self.num_heads, B, self.head_dim), sentinel, dtype=np.float32)
+        pool = np.full((self.num_blocks, self.kv_heads, B, self.head_dim), sentinel, dtype=np.float32)
         for s in range(self.num_seqs):
             ps = int(self.p[s])
             if ps == 0:
@@ -248,7 +258,8 @@ def _assign_blocks(rng: np.random.Generator, ctx: np.ndarray, block_size: int,
 def make_batch(p: Sequence[int], q_len: Sequence[int], *, num_heads: int, head_dim: int,
                block_size: int, dtype: str, seed: int, layer: int = 0,
                num_blocks: Optional[int] = None, permute: bool = True,
-               seq_ids: Optional[Sequence[int]] = None, name: str = "") -> RaggedBatch:
+               seq_ids: Optional[Sequence[int]] = None, name: str = "",
+               num_kv_heads: Optional[int] = None) -> RaggedBatch:
     p = np.asarray(p, dtype=np.int64)
     q_len = np.asarray(q_len, dtype=np.int64)
     rng = np.random.Generator(np.random.PCG64(seed + 7919))
@@ -258,7 +269,7 @@ def make_batch(p: Sequence[int], q_len: Sequence[int], *, num_heads: int, head_d
     return RaggedBatch(num_heads=num_heads, head_dim=head_dim, block_size=block_size,
                        dtype=dtype, seed=seed, layer=layer,
                        seq_ids=np.asarray(seq_ids, dtype=np.int64), p=p, q_len=q_len,
-                       block_tables=bt, num_blocks=nb, name=name)
+                       block_tables=bt, num_blocks=nb, name=name, num_kv_heads=num_kv_heads)
 
 
 def padded_equivalent(b: RaggedBatch) -> RaggedBatch:
@@ -303,25 +314,28 @@ def tiny_fp32(seed: int = 0) -> RaggedBatch:
 
 
 def decode_step(seed: int = 1, num_seqs: int = 256, ctx_lo: int = 512, ctx_hi: int = 4096,
-                num_heads: int = 32, head_dim: int = 128, block_size: int = 16) -> RaggedBatch:
+                num_heads: int = 32, head_dim: int = 128, block_size: int = 16,
+                num_kv_heads: Optional[int] = None) -> RaggedBatch:
     """Decode-only step: every sequence has p ~ U{ctx_lo..ctx_hi} cached tokens and
     one query; blocks drawn from a randomly permuted pool."""
     rng = np.random.Generator(np.random.PCG64(seed))
     p = rng.integers(ctx_lo, ctx_hi, size=num_seqs, endpoint=True)
     return make_batch(p, np.ones(num_seqs, np.int64), num_heads=num_heads, head_dim=head_dim,
-                      block_size=block_size, dtype="bf16", seed=seed, name="decode")
+                      block_size=block_size, dtype="bf16", seed=seed, name="decode",
+                      num_kv_heads=num_kv_heads)
 
 
 def mixed_step(seed: int = 2, num_decode: int = 64, ctx_lo: int = 256, ctx_hi: int = 4096,
                chunks: Sequence[int] = (661, 661, 662), chunk_p: Sequence[int] = (0, 1024, 2048),
-               num_heads: int = 32, head_dim: int = 128, block_size: int = 16) -> RaggedBatch:
+               num_heads: int = 32, head_dim: int = 128, block_size: int = 16,
+               num_kv_heads: Optional[int] = None) -> RaggedBatch:
     """Mixed step, token budget 2048: decode tokens first, then prefill chunks."""
     rng = np.random.Generator(np.random.PCG64(seed))
     pd = rng.integers(ctx_lo, ctx_hi, size=num_decode, endpoint=True)
     p = np.concatenate([pd, np.asarray(chunk_p, np.int64)])
     q = np.concatenate([np.ones(num_decode, np.int64), np.asarray(chunks, np.int64)])
     return make_batch(p, q, num_heads=num_heads, head_dim=head_dim, block_size=block_size,
-                      dtype="bf16", seed=seed, name="mixed")
+                      dtype="bf16", seed=seed, name="mixed", num_kv_heads=num_kv_heads)
 
 
 def long_prompt_chunk(k: int, seed: int = 3, prompt: int = 32768, chunk: int = 2048,

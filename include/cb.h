@@ -128,6 +128,28 @@ cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Grouped-query attention (GQA / MQA): fewer key/value heads than query heads.
+ * The pages have no counterpart; every page assumes one key/value head per
+ * query head.  Here q and out have num_q_heads heads, the cache (and k_new,
+ * v_new of cb_append_kv) cache->num_heads = H_kv heads, num_q_heads a
+ * multiple of H_kv, and query head h attends with key/value head
+ * h / (num_q_heads / H_kv) (groups of consecutive query heads).  Otherwise
+ * identical to cb_ragged_attention, which is the case num_q_heads = H_kv.
+ * A decode unit covers up to four query heads of one group, so each K/V byte
+ * read from memory serves all of them.  Grouped heads need bf16 and a block
+ * size that is a multiple of 16 (CB_ERR_UNSUPPORTED otherwise); the workspace
+ * must be cb_attention_workspace_size_gqa bytes.
+ * ------------------------------------------------------------------------- */
+size_t cb_attention_workspace_size_gqa(const cb_kv_cache* cache, int32_t num_q_heads,
+                                       int32_t num_seqs, int32_t num_tokens, int32_t max_context_len);
+cb_status cb_ragged_attention_gqa(const void* q, int32_t num_q_heads, const cb_kv_cache* cache,
+                                  const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                  const int32_t* block_tables, int32_t num_seqs, int32_t num_tokens,
+                                  int32_t max_blocks_per_seq, int32_t max_q_len,
+                                  int32_t max_context_len, float scale, void* out,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Planned steps and CUDA-graph capture.
  * Hugging Face blog "Continuous batching from first principles", section
  * "Continuous batching": every layer of a step sees the same packed batch, and

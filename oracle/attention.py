@@ -21,6 +21,10 @@ the step sees keys j = 0 .. p+i, and
     o_i = sum_j exp(z_j - max z) v_j / sum_j exp(z_j - max z),  z_j = scale * q_i . k_j
 
 The pages print scores without a scale; the 1/sqrt(A) scale is an input here.
+
+Grouped-query attention (fewer key/value heads than query heads) is not on the
+pages; it is taken as the usual grouping: with H query and H_kv key/value
+heads, query head h uses key/value head h // (H / H_kv).
 """
 from __future__ import annotations
 
@@ -50,8 +54,9 @@ def attend_sequence(q: np.ndarray, k: np.ndarray, v: np.ndarray, p: int, scale: 
                     rows_per_pass: int = 256) -> np.ndarray:
     """Attention of one sequence's new queries over its keys/values.
 
-    q: [n, H, A] this step's queries; k, v: [p + n, H, A] the whole history in
-    token order (cache then new tokens).  Returns [n, H, A] fp64.  Each row's
+    q: [n, H, A] this step's queries; k, v: [p + n, H_kv, A] the whole history
+    in token order (cache then new tokens), H a multiple of H_kv (query head h
+    reads key/value head h // (H / H_kv)).  Returns [n, H, A] fp64.  Each row's
     softmax is taken over its full set of visible keys at once; ``rows_per_pass``
     only bounds memory.
     """
@@ -59,14 +64,17 @@ def attend_sequence(q: np.ndarray, k: np.ndarray, v: np.ndarray, p: int, scale: 
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     n, H, A = q.shape
-    c = k.shape[0]
+    c, H_kv = k.shape[0], k.shape[1]
     if c != p + n or v.shape[0] != c:
         raise ValueError("history length must equal p + q_len")
+    if H_kv < 1 or H % H_kv != 0 or v.shape[1] != H_kv:
+        raise ValueError("query heads must be a multiple of key/value heads")
+    group = H // H_kv
     out = np.empty((n, H, A), dtype=np.float64)
     key_idx = np.arange(c)
     for h in range(H):
-        kh = k[:, h, :]
-        vh = v[:, h, :]
+        kh = k[:, h // group, :]
+        vh = v[:, h // group, :]
         for r0 in range(0, n, rows_per_pass):
             r1 = min(n, r0 + rows_per_pass)
             z = scale * (q[r0:r1, h, :] @ kh.T)                       # [rows, c]
@@ -82,7 +90,7 @@ def ragged_attention(q_packed: np.ndarray, cu_seqlens_q: np.ndarray, context_len
                      k_hist, v_hist, scale: float) -> np.ndarray:
     """Attention over a packed batch, each sequence computed alone and unpacked.
 
-    q_packed: [T, H, A]; k_hist[s], v_hist[s]: [context_lens[s], H, A], the
+    q_packed: [T, H, A]; k_hist[s], v_hist[s]: [context_lens[s], H_kv, A], the
     sequence's full history (the oracle's own record, never a device cache).
     Returns [T, H, A] fp64 in packed order.
     """

@@ -38,7 +38,7 @@ def host_pool_bits(b: W.RaggedBatch, kind: int) -> np.ndarray:
     """Initial pool bits: each sequence's cached prefix at its slots, sentinel NaN elsewhere."""
     sent = BF16_NAN if b.dtype == "bf16" else F32_NAN
     dt = np.uint16 if b.dtype == "bf16" else np.uint32
-    bits = np.full((b.num_blocks, b.num_heads, b.block_size, b.head_dim), sent, dtype=dt)
+    bits = np.full((b.num_blocks, b.kv_heads, b.block_size, b.head_dim), sent, dtype=dt)
     for s in range(b.num_seqs):
         ps = int(b.p[s])
         if ps:
@@ -75,7 +75,7 @@ class DeviceStep:
         self.b = b
         dt = TORCH_DT[b.dtype]
         if cache is None:
-            cache = api.KVCache.empty(b.num_blocks, b.num_heads, b.block_size, b.head_dim, dt)
+            cache = api.KVCache.empty(b.num_blocks, b.kv_heads, b.block_size, b.head_dim, dt)
             fill_sentinel(cache.k)
             fill_sentinel(cache.v)
             self._prefill_cache(cache, source)
@@ -90,8 +90,8 @@ class DeviceStep:
             pos = np.concatenate([np.arange(b.p[s], b.p[s] + b.q_len[s]) for s in range(b.num_seqs)])
             sid = torch.from_numpy(seq_rows.astype(np.int64)).cuda()
             ps = torch.from_numpy(pos.astype(np.int32)).cuda()
-            shape = (T, b.num_heads, b.head_dim)
-            self.q, self.k_new, self.v_new = (torch.empty(shape, dtype=dt, device="cuda") for _ in range(3))
+            self.q, self.k_new, self.v_new = (torch.empty((T, b.heads_of(kind), b.head_dim), dtype=dt, device="cuda")
+                                              for kind in (W.KIND_Q, W.KIND_K, W.KIND_V))
             for kind, t in ((W.KIND_Q, self.q), (W.KIND_K, self.k_new), (W.KIND_V, self.v_new)):
                 api.cb_synth_tokens(t, b.seed, kind, b.layer, sid, ps)
         self.cu = torch.from_numpy(b.cu_seqlens_q).cuda()
@@ -100,7 +100,9 @@ class DeviceStep:
         self.slots = torch.from_numpy(b.slot_mapping).cuda()
         self.out = torch.empty_like(self.q)
         fill_sentinel(self.out)
-        ws = api.cb_attention_workspace_size(self.cache, b.num_seqs, T, b.max_context_len)
+        self.grouped = b.num_heads != b.kv_heads
+        ws = (api.cb_attention_workspace_size_gqa(self.cache, b.num_heads, b.num_seqs, T, b.max_context_len)
+              if self.grouped else api.cb_attention_workspace_size(self.cache, b.num_seqs, T, b.max_context_len))
         self.ws = torch.empty(ws, dtype=torch.uint8, device="cuda")
         self.scale = 1.0 / math.sqrt(b.head_dim)
 
@@ -124,9 +126,9 @@ class DeviceStep:
 
     def attend(self):
         b = self.b
-        api.cb_ragged_attention(self.q, self.cache, self.cu, self.ctx, self.bt,
-                                max_q_len=b.max_q_len, max_context_len=b.max_context_len,
-                                scale=self.scale, out=self.out, workspace=self.ws)
+        fn = api.cb_ragged_attention_gqa if self.grouped else api.cb_ragged_attention
+        fn(self.q, self.cache, self.cu, self.ctx, self.bt, max_q_len=b.max_q_len,
+           max_context_len=b.max_context_len, scale=self.scale, out=self.out, workspace=self.ws)
 
     def run(self):
         self.append()
@@ -143,8 +145,10 @@ def oracle_rows(b: W.RaggedBatch, s: int, heads=None, rows=None) -> np.ndarray:
     pos = np.arange(p, p + n) if rows is None else p + np.asarray(rows)
     c = int(b.context_lens[s]) if rows is None else int(p + np.max(rows) + 1)
     q = W.token_values(b.seed, W.KIND_Q, b.layer, int(b.seq_ids[s]), pos, heads, b.head_dim, b.dtype)
-    k = W.token_values(b.seed, W.KIND_K, b.layer, int(b.seq_ids[s]), np.arange(c), heads, b.head_dim, b.dtype)
-    v = W.token_values(b.seed, W.KIND_V, b.layer, int(b.seq_ids[s]), np.arange(c), heads, b.head_dim, b.dtype)
+    # the key/value head of each query head (one per query head: the oracle then needs no grouping)
+    kvh = [h // (b.num_heads // b.kv_heads) for h in heads]
+    k = W.token_values(b.seed, W.KIND_K, b.layer, int(b.seq_ids[s]), np.arange(c), kvh, b.head_dim, b.dtype)
+    v = W.token_values(b.seed, W.KIND_V, b.layer, int(b.seq_ids[s]), np.arange(c), kvh, b.head_dim, b.dtype)
     if rows is None:
         return oa.attend_sequence(q, k, v, p, 1.0 / math.sqrt(b.head_dim))
     # selected rows: row r sees keys 0..p+r; run each as a one-row chunk at its own offset

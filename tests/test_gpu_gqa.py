@@ -1,0 +1,59 @@
+"""Grouped-query attention (fewer key/value heads than query heads; not on the
+pages): query head h attends with key/value head h // (H / H_kv).  Decode rows
+(units of up to four query heads sharing one K/V stream), prefill chunks and
+mixed steps against the oracle, for groups of 2, 3, 4 and 8 heads and for one
+key/value head (MQA)."""
+import numpy as np
+import pytest
+import torch
+
+from continuous_batching_ragged_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(8, 2), (8, 1), (12, 4), (16, 2), (6, 6)]
+
+
+@pytest.mark.parametrize("H,Hkv", SHAPES)
+def test_gqa_decode_prefill_and_mixed(native_lib, H, Hkv):
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_packed, to_np
+    # decode rows around split and block edges, prefill chunks around tile edges, one mixed step
+    p = [0, 1, 511, 512, 2047, 4100, 300, 0, 129]
+    q = [1, 1, 1, 1, 1, 1, 200, 129, 300]
+    b = W.make_batch(p, q, num_heads=H, head_dim=128, block_size=16, dtype="bf16", seed=200 + H + Hkv,
+                     num_kv_heads=Hkv)
+    got = to_np(DeviceStep(b).run())
+    assert_tolerance(got, oracle_packed(b))
+
+
+def test_gqa_decode_full_size_sampled(native_lib):
+    """The decode workload with 32 query and 8 key/value heads: 256 sequences,
+    contexts 512-4096; sampled (sequence, head) rows against the oracle."""
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_rows, to_np
+    b = W.decode_step(num_kv_heads=8)
+    st = DeviceStep(b, source="device")
+    out = to_np(st.run())
+    rng = np.random.default_rng(3)
+    got, exp = [], []
+    for s in rng.choice(b.num_seqs, 12, replace=False):
+        heads = sorted(rng.choice(32, 4, replace=False).tolist())
+        exp.append(oracle_rows(b, int(s), heads)[0])
+        got.append(out[int(b.cu_seqlens_q[s])][heads])
+    assert_tolerance(np.stack(got), np.stack(exp))
+
+
+def test_gqa_head_groups_do_not_leak(native_lib):
+    """Changing key/value head 0 changes exactly the outputs of query heads in
+    group 0, bit for bit everywhere else."""
+    from continuous_batching_ragged_gb300 import api
+    from gpu_harness import DeviceStep
+    H, Hkv = 8, 2
+    b = W.make_batch([700, 0, 40], [1, 150, 1], num_heads=H, head_dim=128, block_size=16, dtype="bf16",
+                     seed=77, num_kv_heads=Hkv)
+    st = DeviceStep(b)
+    base = st.run().clone()
+    st.cache.k[:, 0] = st.cache.k[:, 0] * -1.5
+    st.attend()
+    api.cb_check_device_errors()
+    changed = [not torch.equal(st.out[:, h].view(torch.int16), base[:, h].view(torch.int16)) for h in range(H)]
+    assert changed == [h // (H // Hkv) == 0 for h in range(H)]

@@ -249,3 +249,31 @@ def test_rows_per_pass_only_bounds_memory():
     a = oa.attend_sequence(q, k, v, 30, 0.5, rows_per_pass=7)
     b = oa.attend_sequence(q, k, v, 30, 0.5, rows_per_pass=256)
     np.testing.assert_allclose(a, b, rtol=1e-14, atol=1e-15)
+
+
+def test_grouped_query_attention_equals_heads_with_repeated_keys_values():
+    """Grouped-query attention (not on the pages; query head h reads key/value
+    head h // G) is multi-head attention whose keys and values are each
+    repeated for the G query heads of their group."""
+    rng = np.random.default_rng(31)
+    for H, H_kv in ((8, 2), (6, 3), (4, 1), (5, 5)):
+        n, p, A = 5, 9, 16
+        q = rng.standard_normal((n, H, A))
+        k = rng.standard_normal((p + n, H_kv, A))
+        v = rng.standard_normal((p + n, H_kv, A))
+        got = oa.attend_sequence(q, k, v, p, 0.25)
+        G = H // H_kv
+        exp = oa.attend_sequence(q, np.repeat(k, G, axis=1), np.repeat(v, G, axis=1), p, 0.25)
+        np.testing.assert_array_equal(got, exp)
+        # and head h's output depends only on its own group's keys and values
+        k2 = k.copy()
+        k2[:, 0] += 1.0
+        changed = np.any(oa.attend_sequence(q, k2, v, p, 0.25) != got, axis=(0, 2))
+        assert changed.tolist() == [h // G == 0 for h in range(H)]
+
+
+def test_grouped_query_attention_rejects_uneven_groups():
+    q = np.zeros((1, 6, 4))
+    k = np.zeros((1, 4, 4))
+    with pytest.raises(ValueError):
+        oa.attend_sequence(q, k, k, 0, 1.0)
