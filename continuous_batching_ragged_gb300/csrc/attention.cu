@@ -9,8 +9,8 @@
 // a dense contraction.  A one-CTA plan kernel first lists the step's work
 // units on the GPU; both attention kernels are persistent grids that claim
 // those units, so the launch shape does not depend on the batch.  In a mixed
-// step the two run on two streams joined by events, and whichever finishes
-// its list first leaves its SMs to the other.  fp32 caches take the CUDA-core
+// step the prefill kernel keeps the share of SMs the plan gives it and the
+// decode kernel takes the rest, side by side.  fp32 caches take the CUDA-core
 // kernel for every row.
 #include <cmath>
 #include <mutex>
@@ -112,24 +112,18 @@ cb_status prepare(const char* who, const void* q, const cb_kv_cache* cache, cons
   return CB_OK;
 }
 
-// Prefill chunks on the auxiliary stream, decode rows on `main`, joined.
-cb_status run_both(const cb::AttnArgs& a, const cb::StepPlan& plan, cudaStream_t main) {
-  cb::AuxStream* aux = cb::aux_stream();
-  if (!aux) return CB_ERR_CUDA;
-  cb::lock_aux();
-  cudaError_t e = cudaEventRecord(aux->fork, main);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(aux->stream, aux->fork, 0);
-  if (e != cudaSuccess) {
-    cb::unlock_aux();
-    return cb::cuda_fail(e, "forking the auxiliary stream");
-  }
-  cb_status sp = cb::launch_prefill_tc(a, plan, false, aux->stream);
-  cb_status sd = cb::launch_decode_persistent(a, plan, false, main);
-  e = cudaEventRecord(aux->join, aux->stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(main, aux->join, 0);
-  cb::unlock_aux();
-  if (e != cudaSuccess) return cb::cuda_fail(e, "joining the auxiliary stream");
-  return sp != CB_OK ? sp : sd;
+// A mixed step on one stream: the prefill kernel, then the decode kernel as a
+// programmatic dependent launch.  Each prefill CTA releases its dependents
+// once it has read the plan, and those beyond the plan's SM share exit at
+// once.  So the decode grid starts on every SM the prefill does not keep,
+// and the two run side by side (a prefill CTA's shared memory leaves no room
+// for a decode CTA on its SM).  Planned steps, made to be captured in CUDA
+// graphs, keep prefill on every SM: a captured step was measured to run the
+// two kernels one after the other, so a share would only slow the prefill.
+cb_status run_both(const cb::AttnArgs& a, const cb::StepPlan& plan, bool after_plan, cudaStream_t main) {
+  cb_status st = cb::launch_prefill_tc(a, plan, after_plan, main);
+  if (st != CB_OK) return st;
+  return cb::launch_decode_persistent(a, plan, true, false, main);
 }
 
 // Plans built by cb_plan_step, by workspace: what the planned attention calls
@@ -167,11 +161,14 @@ cb_status attention(const char* who, const void* q, int32_t num_q_heads, const c
   if (st != CB_OK) return st;
   plan.dec_ctas = cb::decode_persistent_ctas(a);
   plan.dec_groups = a.num_heads / cb::decode_group_heads(a);
+  plan.kv_bytes_per_key = 2 * a.num_kv_heads * a.head_dim * 2;
+  plan.dec_bytes_per_us_per_sm = cb::decode_rate_per_sm(cb::decode_group_heads(a));
+  plan.split_sms = 1;
   st = cb::launch_plan(a, plan, main);
   if (st != CB_OK) return st;
-  if (max_q_len == 1) return cb::launch_decode_persistent(a, plan, true, main);
+  if (max_q_len == 1) return cb::launch_decode_persistent(a, plan, true, true, main);
   if (max_q_len == num_tokens && num_seqs == 1) return cb::launch_prefill_tc(a, plan, true, main);
-  return run_both(a, plan, main);
+  return run_both(a, plan, true, main);
 }
 
 }  // namespace
@@ -231,6 +228,8 @@ extern "C" cb_status cb_plan_step(const cb_kv_cache* cache, const int32_t* cu_se
   if (st != CB_OK) return st;
   rec.plan.dec_ctas = cb::decode_persistent_ctas(a);
   rec.plan.dec_groups = a.num_heads / cb::decode_group_heads(a);
+  rec.plan.kv_bytes_per_key = 2 * a.num_kv_heads * a.head_dim * 2;
+  rec.plan.dec_bytes_per_us_per_sm = cb::decode_rate_per_sm(cb::decode_group_heads(a));
   st = cb::launch_plan(a, rec.plan, static_cast<cudaStream_t>(stream));
   if (st != CB_OK) return st;
   rec.cu = cu_seqlens_q;
@@ -281,5 +280,5 @@ extern "C" cb_status cb_ragged_attention_planned(const void* q, const cb_kv_cach
   // the claim counters start at zero for every call over the plan
   cudaError_t e = cudaMemsetAsync(rec.plan.header + 2, 0, 2 * sizeof(int32_t), main);
   if (e != cudaSuccess) return cb::cuda_fail(e, "clearing the claim counters");
-  return run_both(a, rec.plan, main);
+  return run_both(a, rec.plan, false, main);
 }

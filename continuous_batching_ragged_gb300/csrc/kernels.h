@@ -50,7 +50,8 @@ constexpr int kPrefillPairRows = 256;
 // caller's workspace.
 struct StepPlan {
   int32_t* header;        // [0] decode items, [1] prefill units, [2] decode claims, [3] prefill claims,
-                          // [4] call tag, [5] keys per decode split, [6] num_seqs, [7] num_tokens
+                          // [4] call tag, [5] keys per decode split, [6] num_seqs, [7] num_tokens,
+                          // [8] prefill CTAs that work (the rest leave their SMs to decode)
   int2* dec_items;        // (sequence, split) of every q_len == 1 row, longest first
   int2* dec_scratch;      // the decode items before sorting
   int2* pre_seqs;         // (sequence, query pairs) of every q_len > 1 chunk, costliest chunk first
@@ -65,7 +66,16 @@ struct StepPlan {
   uint32_t tag;           // this call's tag: the plan writes it to header[4], the kernels check it
   int32_t dec_ctas;       // CTAs of the persistent decode grid (sets the split length)
   int32_t dec_groups;     // decode units per decode item (query-head groups)
+  int32_t num_sms;        // SMs of the device (sets the prefill CTAs of a mixed step)
+  int32_t kv_bytes_per_key;  // K and V bytes of one key over all key/value heads
+  float dec_bytes_per_us_per_sm;  // decode K/V bytes one SM streams per microsecond
+  int32_t split_sms;      // 1: a mixed step may give prefill only a share of the SMs (the
+                          // decode kernel then starts behind it as a dependent launch)
 };
+// Decode K/V bytes one SM streams per microsecond when each unit serves
+// `group_heads` query heads (measured on GB300: ~90 GB/s for one head, where
+// memory binds; ~32 GB/s for four, where the arithmetic does).
+float decode_rate_per_sm(int group_heads);
 
 // Workspace of a bf16 step (plan + split scratch) and its carving.
 size_t step_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_heads, int32_t head_dim,
@@ -85,10 +95,13 @@ int decode_persistent_ctas(const AttnArgs& a);
 int decode_group_heads(const AttnArgs& a);
 
 // Persistent decode over the plan's decode items (bf16, head_dim 128, block
-// size a multiple of 16).  `after_plan`: launched right behind launch_plan on
-// the same stream, overlapping its launch with the plan.
-cb_status launch_decode_persistent(const AttnArgs& a, const StepPlan& plan, bool after_plan,
-                                   cudaStream_t stream);
+// size a multiple of 16).  `after_previous`: a programmatic dependent launch
+// behind the kernel launched just before on the same stream; `wait_previous`:
+// the kernel waits for that one to finish before reading the plan (false
+// when it is the prefill kernel, which releases its dependents only after
+// the plan it follows is complete).
+cb_status launch_decode_persistent(const AttnArgs& a, const StepPlan& plan, bool after_previous,
+                                   bool wait_previous, cudaStream_t stream);
 
 // Split-KV attention on CUDA cores.  Decode mode: one query row per sequence
 // with q_len == 1 (other sequences are left to the prefill kernel).  Row mode:

@@ -30,6 +30,18 @@ constexpr int kPlanThreads = 256;
 constexpr int kCostBuckets = 4096;     // costs at or above the last bucket share it
 constexpr int kUnitsPerCta = 6;        // decode units per persistent CTA the split size aims for
 constexpr int kRowCache = 2048;        // rows whose (q_len, ctx) stay in shared memory after pass 1
+// Cost model of a mixed step's SM split, fitted on GB300 to the long-prompt
+// chunk and to %globaltimer stamps of the mixed step's two kernels running
+// side by side: a prefill unit costs about 2.75 us plus 1.1 us per (KV tile x
+// query tile) on one SM; decode streams K/V at about 6.5 TB/s overall, and at
+// most at the per-SM rate the host passes (lower when a unit serves several
+// query heads: then the decode kernel is bound by its arithmetic, not by
+// memory).  A split is taken only if it beats the two kernels one after the
+// other (prefill on every SM, then decode) by kSplitGain.
+constexpr float kPrefillUsPerUnit = 2.75f;
+constexpr float kPrefillUsPerCost = 1.1f;
+constexpr float kDecodeBytesPerUs = 6.5e6f;
+constexpr float kSplitGain = 0.9f;
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -240,13 +252,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
             bucket, warp_sums);
   const int unit_cap = p.pre_cap * a.num_heads;
   uint64_t unit_base = 0;                   // first unit of each sorted chunk, into pre_scratch[].x
+  uint64_t pre_cost = 0;                    // sum of unit costs (KV tiles x query tiles) over all heads
   for (int c0 = 0; c0 < n_chunks; c0 += kPlanThreads) {
     const int c = c0 + tid;
-    const uint32_t n = c < n_chunks ? uint32_t(p.pre_seqs[c].y) * uint32_t(a.num_heads) : 0u;
+    uint32_t n = 0, cost = 0;
+    if (c < n_chunks) {
+      const int2 rec = p.pre_seqs[c];
+      const int2 r = row(rec.x);
+      n = uint32_t(rec.y) * uint32_t(a.num_heads);
+      for (int qp = 0; qp < rec.y; ++qp) cost += uint32_t(pair_cost(r.x, r.y, qp));
+      const uint64_t all_heads = uint64_t(cost) * uint64_t(a.num_heads);
+      cost = all_heads < 0x7FFFFFFFull ? uint32_t(all_heads) : 0x7FFFFFFFu;
+    }
     uint64_t total;
-    const uint64_t off = unit_base + block_excl_scan(n, warp_sums, total);
-    unit_base += total;
-    if (c < n_chunks) p.pre_scratch[c] = make_int2(off < uint64_t(unit_cap) ? int(off) : unit_cap, 0);
+    const uint64_t off = unit_base + block_excl_scan(uint64_t(n) | (uint64_t(cost) << 32), warp_sums, total);
+    unit_base += uint64_t(uint32_t(total));
+    pre_cost += total >> 32;
+    const uint64_t off_units = uint32_t(off);
+    if (c < n_chunks) p.pre_scratch[c] = make_int2(off_units < uint64_t(unit_cap) ? int(off_units) : unit_cap, 0);
   }
   if (unit_base > uint64_t(unit_cap) && tid == 0) raise_error(a.err, kErrInvalid);
   const int n_pre_units = int(unit_base < uint64_t(unit_cap) ? unit_base : uint64_t(unit_cap));
@@ -263,6 +286,36 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
     const int h = local / rec.y, k = local - h * rec.y;
     p.pre_units[i] = make_int2(rec.x, (rec.y - 1 - k) | (h << 16));
   }
+  // SMs for prefill in a mixed step: prefill on k SMs and decode on the rest
+  // run side by side; each thread scores one k (k = tid + 1), the block keeps
+  // the best (estimated step time, then the smaller k)
+  int k = p.num_sms;
+  {
+    const float dec_bytes = float(total_keys) * float(p.kv_bytes_per_key);
+    if (p.split_sms && n_pre_units > 0 && dec_bytes > 0.f && p.num_sms > 1) {
+      const float pre_us = float(n_pre_units) * kPrefillUsPerUnit + float(pre_cost) * kPrefillUsPerCost;  // one SM
+      const float serial = __fdividef(pre_us, float(p.num_sms)) +
+                           __fdividef(dec_bytes, fminf(kDecodeBytesPerUs, p.dec_bytes_per_us_per_sm * p.num_sms));
+      float score = 3.0e38f;
+      const int kk = tid + 1;
+      if (kk < p.num_sms) {
+        const float bw = fminf(kDecodeBytesPerUs, p.dec_bytes_per_us_per_sm * float(p.num_sms - kk));
+        score = fmaxf(__fdividef(pre_us, float(kk)), __fdividef(dec_bytes, bw));
+      }
+      // (score, k) minimum: scores are positive floats, so their bits order like the floats
+      uint64_t key = (uint64_t(__float_as_uint(score)) << 32) | uint32_t(kk);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, key, o);
+        key = other < key ? other : key;
+      }
+      if ((tid & 31) == 0) warp_sums[tid >> 5] = key;
+      __syncthreads();
+      uint64_t best = warp_sums[0];
+      for (int w = 1; w < kPlanThreads / 32; ++w) best = warp_sums[w] < best ? warp_sums[w] : best;
+      if (__uint_as_float(uint32_t(best >> 32)) < kSplitGain * serial) k = int(uint32_t(best));
+    }
+  }
   if (tid == 0) {
     p.header[0] = n_dec;
     p.header[1] = n_pre_units;
@@ -272,6 +325,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
     p.header[5] = split;
     p.header[6] = z.num_seqs;
     p.header[7] = z.num_tokens;
+    p.header[8] = k;
   }
 }
 
@@ -321,6 +375,10 @@ cb_status step_plan_layout(void* workspace, size_t workspace_bytes, int32_t num_
   plan->pre_cap = int32_t(pre_cap);
   plan->dec_ctas = 0;
   plan->dec_groups = 0;
+  plan->num_sms = sm_count();
+  plan->kv_bytes_per_key = 0;
+  plan->dec_bytes_per_us_per_sm = 9.0e4f;
+  plan->split_sms = 0;
   static std::atomic<uint32_t> next_tag{1};
   plan->tag = next_tag.fetch_add(1);
   return CB_OK;

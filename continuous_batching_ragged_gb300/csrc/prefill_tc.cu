@@ -230,11 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependency_wait();                          // the plan kernel has finished
   const uint32_t seen_tag = uint32_t(__ldcg(w.header + 4));
   int n_units = __ldcg(w.header + 1);
+  int working = __ldcg(w.header + 8);              // CTAs that take units; the others leave their SM
   if (seen_tag != w.tag || n_units < 0 || n_units > w.unit_cap) {   // a list from another call: no work
     if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(a.err, kErrInvalid);
     n_units = 0;
   }
-  if (int(blockIdx.x) >= n_units) return;          // no unit could be left for this CTA: skip the setup
+  // The plan is complete: a decode kernel launched behind this one may start
+  // now, on the SMs this grid leaves free.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (working < 1) working = gridDim.x;
+  if (int(blockIdx.x) >= min(n_units, working)) return;   // no unit for this CTA: skip the setup
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);

@@ -50,6 +50,7 @@ struct SplitArgs {
   int32_t item_cap;         // persistent decode: capacity of the item list
   uint32_t tag;             // persistent decode: the plan's call tag
   int32_t n_groups;         // persistent decode: units per item (query-head groups)
+  int32_t wait_previous;    // persistent decode: wait for the kernel launched before (the plan)
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const 
     sm100::fence_mbar_init();
   }
   if (threadIdx.x == 0) abort_flag = 0;
-  grid_dependency_wait();                   // the plan kernel has finished
+  if (sa.wait_previous) grid_dependency_wait();   // the plan kernel has finished
   const int H = a.num_heads;                // query heads
   const int G = H / a.num_kv_heads;         // query heads per KV head
   const int n_groups = sa.n_groups;         // = H / GU
@@ -669,6 +670,15 @@ int decode_group_heads(const AttnArgs& a) {
   return 1;
 }
 
+float decode_rate_per_sm(int group_heads) {
+  switch (group_heads) {
+    case 1: return 9.0e4f;
+    case 2: return 6.0e4f;
+    case 3: return 4.2e4f;
+    default: return 3.2e4f;
+  }
+}
+
 template <int GU>
 static int persistent_ctas(int dev) {
   static int ctas_per_sm[64] = {};
@@ -708,8 +718,9 @@ static bool persistent_ok(const AttnArgs& a) {
 }
 
 cb_status launch_decode_persistent(const AttnArgs& a, const StepPlan& plan, bool after_plan,
-                                   cudaStream_t stream) {
+                                   bool wait_previous, cudaStream_t stream) {
   SplitArgs sa;
+  sa.wait_previous = wait_previous ? 1 : 0;
   sa.a = a;
   sa.tickets = plan.tickets;
   sa.partials = plan.partials;
@@ -775,9 +786,11 @@ cb_status launch_split_kv(const AttnArgs& a, bool row_mode, void* workspace,
     if (st != CB_OK) return st;
     plan.dec_ctas = decode_persistent_ctas(a);
     plan.dec_groups = a.num_heads / decode_group_heads(a);
+    plan.kv_bytes_per_key = 2 * a.num_kv_heads * a.head_dim * (a.dtype == CB_DTYPE_BF16 ? 2 : 4);
+    plan.dec_bytes_per_us_per_sm = decode_rate_per_sm(decode_group_heads(a));
     st = launch_plan(a, plan, stream);
     if (st != CB_OK) return st;
-    return launch_decode_persistent(a, plan, true, stream);
+    return launch_decode_persistent(a, plan, true, true, stream);
   }
   if (rows > 65535) return fail(CB_ERR_UNSUPPORTED, "split-KV path: more than 65535 rows");
   SplitArgs sa = {};
