@@ -43,6 +43,11 @@ constexpr int kSplitKeys = 512;
 
 // Query rows per prefill unit (two 128-row tiles).
 constexpr int kPrefillPairRows = 256;
+// Partial-result slots for prefill units cut into KV segments: a step is
+// segmented only if its segments fit.
+constexpr int kPrefillSegSlots = 1024;
+// Arrival tickets per partial slot: one per (query tile, softmax warp).
+constexpr int kSegTicketsPerSlot = 8;
 
 // The step's work lists, built on the GPU from the packed metadata by
 // launch_plan and consumed by the persistent decode and prefill kernels, which
@@ -51,18 +56,23 @@ constexpr int kPrefillPairRows = 256;
 struct StepPlan {
   int32_t* header;        // [0] decode items, [1] prefill units, [2] decode claims, [3] prefill claims,
                           // [4] call tag, [5] keys per decode split, [6] num_seqs, [7] num_tokens,
-                          // [8] prefill CTAs that work (the rest leave their SMs to decode)
+                          // [8] prefill CTAs that work (the rest leave their SMs to decode),
+                          // [9] KV tiles per prefill segment (0: units are not segmented)
   int2* dec_items;        // (sequence, split) of every q_len == 1 row, longest first
   int2* dec_scratch;      // the decode items before sorting
   int2* pre_seqs;         // (sequence, query pairs) of every q_len > 1 chunk, costliest chunk first
   int2* pre_scratch;      // the same records before sorting
-  int2* pre_units;        // prefill units (sequence, pair | head << 16): chunk by chunk in
-                          // pre_seqs order, head-major within a chunk, costliest pair first
+  int4* pre_units;        // prefill entries (sequence, pair | head << 16, first | end KV tile << 16,
+                          // partial slot of the unit's first segment or -1), in claim order
+  int32_t* pre_tickets;   // [kPrefillSegSlots][kSegTicketsPerSlot] arrival counters of segmented units
+  float* pre_partials;    // [kPrefillSegSlots][A + 2][256 rows] segment results (acc, max, sum),
+                          // present (else null) when num_tokens > num_seqs and
+                          // max_context_len > 2048
   int32_t* tickets;       // [num_seqs][H] split arrival counters, zeroed by the plan
   float* partials;        // [num_seqs][H][max_splits][A + 2] split results (acc, max, sum)
   int32_t max_splits;
   int32_t dec_cap;        // capacity of dec_items
-  int32_t pre_cap;        // capacity of pre_seqs and pre_scratch (pre_units holds pre_cap * H)
+  int32_t pre_cap;        // capacity of pre_seqs and pre_scratch (pre_units holds pre_cap * H + kPrefillSegSlots)
   uint32_t tag;           // this call's tag: the plan writes it to header[4], the kernels check it
   int32_t dec_ctas;       // CTAs of the persistent decode grid (sets the split length)
   int32_t dec_groups;     // decode units per decode item (query-head groups)

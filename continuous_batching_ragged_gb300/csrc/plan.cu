@@ -42,8 +42,23 @@ constexpr float kPrefillUsPerUnit = 2.75f;
 constexpr float kPrefillUsPerCost = 1.1f;
 constexpr float kDecodeBytesPerUs = 6.5e6f;
 constexpr float kSplitGain = 0.9f;
+// Prefill KV segments: a query pair's keys are cut into segments of L KV
+// tiles when some pair is long next to the work every SM gets (the step's
+// prefill and decode estimates over all SMs), which otherwise leaves a tail
+// of idle SMs: the last 2048-token chunk of a 32768-token prompt is 256 units
+// of ~250 tiles for 152 SMs.  L is 1/kSegPerShare of an SM's share, at least
+// kSegMinTiles.  The choice depends on the step and the SM count only, not on
+// the SM share a mixed step gives prefill, so a step's bits never depend on it.
+constexpr int kSegPerShare = 4;
+constexpr int kSegMinTiles = 16;
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Segment partials exist only where a step could use them: a prefill chunk
+// (T > S) with a context longer than the shortest segment.
+bool has_seg_partials(size_t S, size_t T, int32_t max_context_len) {
+  return T > S && max_context_len > kSegMinTiles * 128;
+}
 
 __device__ __forceinline__ void launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -87,6 +102,14 @@ __device__ __forceinline__ int pair_cost(int q_len, int ctx, int qp) {
   const int nq = row0 + kPrefillPairRows / 2 < q_len ? 2 : 1;
   const int kv_end = min(ctx - q_len + row0 + nq * (kPrefillPairRows / 2), ctx);
   return ((kv_end + 127) / 128) * nq;
+}
+
+// KV tiles that query pair qp of a chunk streams.
+__device__ __forceinline__ int pair_tiles(int q_len, int ctx, int qp) {
+  const int row0 = qp * kPrefillPairRows;
+  const int nq = row0 + kPrefillPairRows / 2 < q_len ? 2 : 1;
+  const int kv_end = min(ctx - q_len + row0 + nq * (kPrefillPairRows / 2), ctx);
+  return (kv_end + 127) / 128;
 }
 
 struct RowInfo {
@@ -273,19 +296,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
   }
   if (unit_base > uint64_t(unit_cap) && tid == 0) raise_error(a.err, kErrInvalid);
   const int n_pre_units = int(unit_base < uint64_t(unit_cap) ? unit_base : uint64_t(unit_cap));
-  __syncthreads();
-  // every thread writes units: unit i belongs to the last chunk starting at or before it
-  for (int i = tid; i < n_pre_units; i += kPlanThreads) {
-    int lo = 0, hi = n_chunks - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.pre_scratch[mid].x <= i) lo = mid; else hi = mid - 1;
-    }
-    const int2 rec = p.pre_seqs[lo];
-    const int local = i - p.pre_scratch[lo].x;
-    const int h = local / rec.y, k = local - h * rec.y;
-    p.pre_units[i] = make_int2(rec.x, (rec.y - 1 - k) | (h << 16));
-  }
   // SMs for prefill in a mixed step: prefill on k SMs and decode on the rest
   // run side by side; each thread scores one k (k = tid + 1), the block keeps
   // the best (estimated step time, then the smaller k)
@@ -316,9 +326,86 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
       if (__uint_as_float(uint32_t(best >> 32)) < kSplitGain * serial) k = int(uint32_t(best));
     }
   }
+
+  // Segments: the length L (KV tiles), then each chunk's entries with it
+  // (pre_scratch[c].y: first entry of chunk c); segments are kept only if
+  // some pair is cut and their partial slots fit
+  int seg = 0;
+  if (p.pre_partials && n_pre_units > 0) {
+    const float pre_us = float(n_pre_units) * kPrefillUsPerUnit + float(pre_cost) * kPrefillUsPerCost;
+    const float dec_us = __fdividef(float(total_keys) * float(p.kv_bytes_per_key), p.dec_bytes_per_us_per_sm);
+    // an SM's share in KV tiles of a two-tile unit
+    const float share = __fdividef(pre_us + dec_us, float(p.num_sms) * 2.0f * kPrefillUsPerCost);
+    const float want = ceilf(__fdividef(share, float(kSegPerShare)));
+    seg = want < float(kSegMinTiles) ? kSegMinTiles : (want > 65535.0f ? 65535 : int(want));
+  }
+  uint64_t n_entries = n_pre_units;
+  if (seg > 0) {
+    uint64_t entry_base = 0;
+    for (int c0 = 0; c0 < n_chunks; c0 += kPlanThreads) {
+      const int c = c0 + tid;
+      uint32_t e = 0;
+      if (c < n_chunks) {
+        const int2 rec = p.pre_seqs[c];
+        const int2 r = row(rec.x);
+        for (int qp = 0; qp < rec.y; ++qp) e += uint32_t((pair_tiles(r.x, r.y, qp) + seg - 1) / seg);
+        e *= uint32_t(a.num_heads);
+      }
+      uint64_t total;
+      const uint64_t off = entry_base + block_excl_scan(e, warp_sums, total);
+      entry_base += total;
+      if (c < n_chunks) p.pre_scratch[c].y = int(off < uint64_t(kPrefillSegSlots) ? off : kPrefillSegSlots);
+    }
+    if (entry_base > uint64_t(n_pre_units) && entry_base <= uint64_t(kPrefillSegSlots)) n_entries = entry_base;
+    else seg = 0;                                          // no pair cut, or too many segments: whole units
+  }
+  for (int i = tid; i < int(seg > 0 ? n_entries * kSegTicketsPerSlot : 0); i += kPlanThreads) p.pre_tickets[i] = 0;
+  __syncthreads();
+  // one thread per unit (chunk, head, pair) writes the unit's entries: unit
+  // u belongs to the last chunk starting at or before it; whole units go
+  // head by head, costliest pair first
+  for (int u = tid; u < n_pre_units; u += kPlanThreads) {
+    int lo = 0, hi = n_chunks - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.pre_scratch[mid].x <= u) lo = mid; else hi = mid - 1;
+    }
+    const int2 rec = p.pre_seqs[lo];
+    const int2 r = row(rec.x);
+    const int np = rec.y;
+    const int local = u - p.pre_scratch[lo].x;
+    const int h = local / np, qp = np - 1 - (local - h * np);
+    const int nt = pair_tiles(r.x, r.y, qp);
+    if (seg == 0) {
+      p.pre_units[u] = make_int4(rec.x, qp | (h << 16), nt << 16, -1);
+      continue;
+    }
+    // Segments: by segment index kk (all heads, then the next index), head
+    // by head, costliest pair first, so the pairs of one head run the same
+    // KV range together.  Pairs later in the chunk have more tiles, so the
+    // cnt pairs with a segment kk are the last ones.  A pair's segments share
+    // its slots [slot0, slot0 + nseg).
+    int per_head = 0, before = 0;
+    for (int q2 = 0; q2 < np; ++q2) {
+      const int ns = (pair_tiles(r.x, r.y, q2) + seg - 1) / seg;
+      per_head += ns;
+      if (q2 < qp) before += ns;
+    }
+    const int e_c = p.pre_scratch[lo].y;
+    const int nseg = (nt + seg - 1) / seg;
+    const int slot0 = nseg > 1 ? e_c + h * per_head + before : -1;
+    int off = 0;
+    for (int kk = 0; kk < nseg; ++kk) {
+      int cnt = 0;
+      for (int q2 = 0; q2 < np; ++q2) cnt += pair_tiles(r.x, r.y, q2) > kk * seg ? 1 : 0;
+      const int j0 = kk * seg, j1 = min(j0 + seg, nt);
+      p.pre_units[e_c + off + h * cnt + (np - 1 - qp)] = make_int4(rec.x, qp | (h << 16), j0 | (j1 << 16), slot0);
+      off += cnt * a.num_heads;
+    }
+  }
   if (tid == 0) {
     p.header[0] = n_dec;
-    p.header[1] = n_pre_units;
+    p.header[1] = int(n_entries);
     p.header[2] = 0;
     p.header[3] = 0;
     p.header[4] = int32_t(p.tag);
@@ -326,6 +413,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
     p.header[6] = z.num_seqs;
     p.header[7] = z.num_tokens;
     p.header[8] = k;
+    p.header[9] = seg;
   }
 }
 
@@ -339,7 +427,11 @@ size_t step_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_he
   return 256 +                                                        // header
          2 * align256(S * splits * sizeof(int2)) +                    // decode items + scratch
          2 * align256(pre_cap * sizeof(int2)) +                       // prefill chunk records + scratch
-         align256(pre_cap * num_heads * sizeof(int2)) +               // prefill units
+         align256((pre_cap * num_heads + kPrefillSegSlots) * sizeof(int4)) +   // prefill entries
+         align256(size_t(kPrefillSegSlots) * kSegTicketsPerSlot * sizeof(int32_t)) +   // segment tickets
+         (has_seg_partials(S, T, max_context_len)                     // prefill segment partials
+              ? size_t(kPrefillSegSlots) * kPrefillPairRows * (head_dim + 2) * sizeof(float)
+              : 0) +
          align256(S * num_heads * sizeof(int32_t)) +                  // tickets
          (splits > 1 ? S * num_heads * splits * (head_dim + 2) * sizeof(float) : 0);   // partials
 }
@@ -365,8 +457,15 @@ cb_status step_plan_layout(void* workspace, size_t workspace_bytes, int32_t num_
   w += align256(pre_cap * sizeof(int2));
   plan->pre_scratch = reinterpret_cast<int2*>(w);
   w += align256(pre_cap * sizeof(int2));
-  plan->pre_units = reinterpret_cast<int2*>(w);
-  w += align256(pre_cap * num_heads * sizeof(int2));
+  plan->pre_units = reinterpret_cast<int4*>(w);
+  w += align256((pre_cap * num_heads + kPrefillSegSlots) * sizeof(int4));
+  plan->pre_tickets = reinterpret_cast<int32_t*>(w);
+  w += align256(size_t(kPrefillSegSlots) * kSegTicketsPerSlot * sizeof(int32_t));
+  plan->pre_partials = nullptr;
+  if (has_seg_partials(S, T, max_context_len)) {
+    plan->pre_partials = reinterpret_cast<float*>(w);
+    w += size_t(kPrefillSegSlots) * kPrefillPairRows * (head_dim + 2) * sizeof(float);
+  }
   plan->tickets = reinterpret_cast<int32_t*>(w);
   w += align256(S * num_heads * sizeof(int32_t));
   plan->partials = reinterpret_cast<float*>(w);

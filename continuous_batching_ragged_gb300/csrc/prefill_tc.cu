@@ -89,11 +89,12 @@ enum : int {
   NUM_BARS = BAR_DONE + 1
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + 8 * NUM_BARS;
-constexpr uint32_t kOffItems = kOffTmemSlot + 16;  // kItemSlots work items of 32 bytes
+constexpr uint32_t kOffItems = kOffTmemSlot + 16;  // kItemSlots work items of 48 bytes
 constexpr int kLookAhead = 4;                    // tiles of block-table look-ahead and L2 prefetch
 constexpr int kRing = 8;                         // box-index ring slots per loader (> kLookAhead)
-constexpr uint32_t kOffRing = kOffItems + kItemSlots * 32;  // two rings (K, V) of kRing x 16 ints
+constexpr uint32_t kOffRing = kOffItems + kItemSlots * 48;  // two rings (K, V) of kRing x 16 ints
 constexpr uint32_t kSmemBytes = kOffRing + 2 * kRing * 16 * 4 + 1024;   // + slack to align the base
+constexpr int kSlotFloats = (HD + 2) * kPrefillPairRows;   // one partial slot: [HD + 2][256 rows]
 static_assert(kRing > kLookAhead, "ring must outlive the look-ahead");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -133,6 +134,107 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// The last-arriving segment of a pair merges its warp's rows (this thread:
+// `rows`, the row in slot 0) over all nseg segments by log-sum-exp, in slot
+// order whoever arrives last, so the bits never depend on timing.  Its own
+// segment `mine` comes from TMEM (o_taddr) and registers, the same fp32
+// values its partial slot would hold; the others from their slots, two slots
+// of 32 dims in flight at a time.  Warp-wide (tcgen05.ld); `store`: this
+// thread's row is a real query row.
+__device__ __forceinline__ void merge_segments(const float* rows, int nseg, int mine, float m_own, float l_own,
+                                               uint32_t o_taddr, __nv_bfloat16* dst, bool store) {
+  constexpr int kM = HD * kPrefillPairRows, kL = (HD + 1) * kPrefillPairRows;
+  float mx = m_own;
+  for (int sg = 0; sg < nseg; ++sg)
+    if (sg != mine) mx = fmaxf(mx, __ldcg(rows + size_t(sg) * kSlotFloats + kM));
+  float sum = 0.f;
+  for (int sg = 0; sg < nseg; ++sg) {
+    const float* src = rows + size_t(sg) * kSlotFloats;
+    sum += sg == mine ? ex2(m_own - mx) * l_own : ex2(__ldcg(src + kM) - mx) * __ldcg(src + kL);
+  }
+  const float inv = 1.0f / sum;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t own[32];
+    tmem_ld32(o_taddr + 32 * c, own);
+    tmem_wait_ld();
+    float acc[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+#pragma unroll 1
+    for (int sg = 0; sg < nseg; sg += 2) {
+      const bool two = sg + 1 < nseg;
+      const float* s0 = rows + size_t(sg) * kSlotFloats;
+      const float* s1 = s0 + kSlotFloats;
+      float v0[32], v1[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        v0[e] = sg == mine ? __uint_as_float(own[e]) : __ldcg(s0 + (32 * c + e) * kPrefillPairRows);
+        v1[e] = !two ? 0.f : (sg + 1 == mine ? __uint_as_float(own[e]) : __ldcg(s1 + (32 * c + e) * kPrefillPairRows));
+      }
+      const float w0 = (sg == mine ? ex2(m_own - mx) : ex2(__ldcg(s0 + kM) - mx)) * inv;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) acc[e] = fmaf(w0, v0[e], acc[e]);
+      if (two) {
+        const float w1 = (sg + 1 == mine ? ex2(m_own - mx) : ex2(__ldcg(s1 + kM) - mx)) * inv;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = fmaf(w1, v1[e], acc[e]);
+      }
+    }
+    if (store) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        d4[e] = make_uint4(pack_bf16x2(acc[8 * e], acc[8 * e + 1]), pack_bf16x2(acc[8 * e + 2], acc[8 * e + 3]),
+                           pack_bf16x2(acc[8 * e + 4], acc[8 * e + 5]), pack_bf16x2(acc[8 * e + 6], acc[8 * e + 7]));
+    }
+  }
+}
+
+// One KV segment of a segmented pair, after its last P V (warp-wide).  One
+// ticket per (pair, query tile, warp): the warp whose segment arrives last
+// merges its 32 rows over every segment, so no warp ever waits on another
+// warp or CTA.  Every other segment first stores its unnormalised rows (acc,
+// max, sum) in its partial slot, dimension-major so a warp's 32 rows are one
+// coalesced line.  `rows`: this thread's row in the pair's first slot.
+__device__ __forceinline__ void segment_epilogue(float* rows, int32_t* ticket, int nseg, int mine, float m, float l,
+                                              uint32_t o_taddr, int lane, __nv_bfloat16* dst, bool store) {
+  int merge = 0;
+  if (lane == 0 && ld_acquire_gpu(ticket) == nseg - 1) {   // the others are in: no partial needed
+    *ticket = 0;                                   // ready for the next call
+    merge = 1;
+  }
+  merge = __shfl_sync(0xffffffffu, merge, 0);
+  if (!merge) {
+    float* slot = rows + size_t(mine) * kSlotFloats;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[32];
+      tmem_ld32(o_taddr + 32 * c, o);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) __stcg(slot + (32 * c + e) * kPrefillPairRows, __uint_as_float(o[e]));
+    }
+    __stcg(slot + HD * kPrefillPairRows, m);
+    __stcg(slot + (HD + 1) * kPrefillPairRows, l);
+    __threadfence();                               // this row's partial is visible before the ticket
+    __syncwarp();
+    if (lane == 0 && atomicAdd(ticket, 1) == nseg - 1) {
+      *ticket = 0;
+      __threadfence();                             // acquire: the other partials are read after this
+      merge = 1;
+    }
+    merge = __shfl_sync(0xffffffffu, merge, 0);
+  }
+  if (merge) merge_segments(rows, nseg, mine, m, l, o_taddr, dst, store);
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t x, int32_t y, int32_t z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z)
@@ -140,9 +242,10 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t x, 
 }
 
 // Warp-wide: lane i < 128/B looks up paged block i of KV tile j in one coalesced
-// load, stores its box index (or `oob`, zero fill) in the ring slot of tile j,
+// load, stores its box index (or `oob`, zero fill) in the ring slot of the
+// piece's jl-th tile,
 // and asks TMA to prefetch that box into L2 for the load a few tiles later.
-__device__ __forceinline__ void stage_boxes(int j, int B, int ctx, const int32_t* bt, const AttnArgs& a,
+__device__ __forceinline__ void stage_boxes(int j, int jl, int B, int ctx, const int32_t* bt, const AttnArgs& a,
                                             int hkv, int lane, int* ring, const CUtensorMap* tm) {
   const int bpt = BN / B;
   if (lane < bpt) {
@@ -158,7 +261,7 @@ __device__ __forceinline__ void stage_boxes(int j, int B, int ctx, const int32_t
         raise_error(a.err, kErrBounds);
       }
     }
-    ring[(j % kRing) * 16 + lane] = z;
+    ring[(jl % kRing) * 16 + lane] = z;
   }
   __syncwarp();
 }
@@ -172,16 +275,19 @@ __device__ __forceinline__ void load_kv_tile_ring(uint32_t dst, const CUtensorMa
   }
 }
 
-// One claimed unit of work: a 256-row query pair of one chunk, one head.
+// One claimed piece of work: KV tiles [j0, j1) of a 256-row query pair of one
+// chunk, one head (the whole pair's range unless the plan cut it into
+// segments, whose results then go to partial slots slot0 + j0 / segment).
 struct WorkItem {
-  int u;                                           // unit index; >= the unit count: no more work
-  int s, h, row0, c0, q_len, ctx, pad;
+  int u;                                           // entry index; >= the entry count: no more work
+  int s, h, row0, c0, q_len, ctx, j0, j1, slot0, pad0, pad1;
 };
-static_assert(sizeof(WorkItem) == 32, "work item slot");
+static_assert(sizeof(WorkItem) == 48, "work item slot");
 
-// Shape of a unit: query tiles holding real rows, KV tiles any row can see.
+// Shape of a piece: query tiles holding real rows, KV tiles any row of the
+// pair can see (the pair's whole range), the piece's first tile and count.
 struct UnitShape {
-  int nq, p, n_tiles;
+  int nq, p, n_tiles, j0, n;
 };
 __device__ __forceinline__ UnitShape unit_shape(const WorkItem& it) {
   UnitShape sh;
@@ -189,6 +295,8 @@ __device__ __forceinline__ UnitShape unit_shape(const WorkItem& it) {
   sh.p = it.ctx - it.q_len;                        // cached tokens before this step
   const int kv_end = min(sh.p + it.row0 + sh.nq * BM, it.ctx);
   sh.n_tiles = (kv_end + BN - 1) / BN;
+  sh.j0 = it.j0;
+  sh.n = it.j1 - it.j0;
   return sh;
 }
 
@@ -197,7 +305,9 @@ __device__ __forceinline__ void grid_dependency_wait() {
 }
 
 struct PrefillWork {
-  const int2* units;        // the plan's units (sequence, query pair | head << 16), in claim order
+  const int4* units;        // the plan's entries (sequence, pair | head << 16, j0 | j1 << 16, slot0)
+  int32_t* tickets;         // arrival counters of segmented pairs: [slot0][query tile * 4 + warp]
+  float* partials;          // [slot][256 rows][HD + 2] segment results (acc, max, sum)
   const int32_t* header;    // [1] = number of units
   int32_t* claims;          // claim counter
   int32_t unit_cap;         // capacity of the unit list
@@ -231,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t seen_tag = uint32_t(__ldcg(w.header + 4));
   int n_units = __ldcg(w.header + 1);
   int working = __ldcg(w.header + 8);              // CTAs that take units; the others leave their SM
+  const int seg = __ldcg(w.header + 9);            // KV tiles per segment (0: whole pairs)
   if (seen_tag != w.tag || n_units < 0 || n_units > w.unit_cap) {   // a list from another call: no work
     if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(a.err, kErrInvalid);
     n_units = 0;
@@ -306,18 +417,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         WorkItem it = {};
         it.u = atomicAdd(w.claims, 1);
         if (it.u < n_units) {
-          const int2 pu = __ldcg(w.units + it.u);
+          const int4 pu = __ldcg(w.units + it.u);
           const int qp = pu.y & 0xFFFF;
           it.s = pu.x;
           it.h = pu.y >> 16;
           it.row0 = qp * kPrefillPairRows;
-          bool bad = it.s < 0 || it.s >= a.num_seqs || it.h < 0 || it.h >= H;
+          it.j0 = pu.z & 0xFFFF;
+          it.j1 = pu.z >> 16;
+          it.slot0 = pu.w;
+          bool bad = it.s < 0 || it.s >= a.num_seqs || it.h < 0 || it.h >= H || it.j1 <= it.j0 ||
+                     (it.slot0 >= 0 && (seg < 1 || it.slot0 >= kPrefillSegSlots || !w.partials));
           if (!bad) {
             it.c0 = __ldcg(a.cu_seqlens_q + it.s);
             it.q_len = __ldcg(a.cu_seqlens_q + it.s + 1) - it.c0;
             it.ctx = __ldcg(a.context_lens + it.s);
             bad = it.c0 < 0 || it.q_len < 2 || it.c0 + it.q_len > a.num_tokens || it.row0 >= it.q_len ||
                   it.ctx < it.q_len || it.ctx > a.max_context_len;
+            if (!bad) {
+              const UnitShape sh = unit_shape(it);
+              bad = it.j1 > sh.n_tiles ||
+                    (it.slot0 >= 0 && (it.j0 % seg != 0 || it.j1 != min(it.j0 + seg, sh.n_tiles) ||
+                                       sh.n_tiles <= seg ||
+                                       it.slot0 + (sh.n_tiles + seg - 1) / seg > kPrefillSegSlots));
+            }
           }
           if (bad) {                               // never happens with a plan from this call
             raise_error(a.err, kErrInvalid);
@@ -347,16 +469,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         return true;
       };
-      const int q_at = min(kKStages - 1, sh.n_tiles);   // K tiles requested before the Q load
-      for (int j = 0; j < min(kLookAhead, sh.n_tiles); ++j)
-        stage_boxes(j, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_k);
-      for (int j = 0; j < sh.n_tiles; ++j) {
+      const int q_at = min(kKStages - 1, sh.n);   // K tiles requested before the Q load
+      for (int j = 0; j < min(kLookAhead, sh.n); ++j)
+        stage_boxes(sh.j0 + j, j, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_k);
+      for (int j = 0; j < sh.n; ++j) {
         if (j == q_at && !load_q()) {
           ok = false;
           site = kSitePfQFree;
           break;
         }
-        if (j + kLookAhead < sh.n_tiles) stage_boxes(j + kLookAhead, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_k);
+        if (j + kLookAhead < sh.n) stage_boxes(sh.j0 + j + kLookAhead, j + kLookAhead, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_k);
         const uint32_t g = kc + j;
         const int st = g % kKStages;
         if (g >= kKStages && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_KE + st), ((g / kKStages) - 1) & 1))) {
@@ -370,12 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      if (ok && q_at == sh.n_tiles && !load_q()) {
+      if (ok && q_at == sh.n && !load_q()) {
         ok = false;
         site = kSitePfQFree;
       }
       if (!ok) break;
-      kc += sh.n_tiles;
+      kc += sh.n;
     }
     if (!ok && lane == 0) raise_error(a.err, kErrTimeout | site);
     if (lane == 0) {
@@ -403,10 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it.u >= n_units) break;
       const UnitShape sh = unit_shape(it);
       const int32_t* bt = a.block_tables + size_t(it.s) * a.max_blocks_per_seq;
-      for (int j = 0; j < min(kLookAhead, sh.n_tiles); ++j)
-        stage_boxes(j, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_v);
-      for (int j = 0; j < sh.n_tiles; ++j) {
-        if (j + kLookAhead < sh.n_tiles) stage_boxes(j + kLookAhead, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_v);
+      for (int j = 0; j < min(kLookAhead, sh.n); ++j)
+        stage_boxes(sh.j0 + j, j, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_v);
+      for (int j = 0; j < sh.n; ++j) {
+        if (j + kLookAhead < sh.n) stage_boxes(sh.j0 + j + kLookAhead, j + kLookAhead, B, it.ctx, bt, a, it.h / G, lane, ring, &tm_v);
         const uint32_t g = vc + j;
         const int st = g % kVStages;
         if (g >= kVStages && !__all_sync(0xffffffffu, mbar_wait(bar(BAR_VE + st), ((g / kVStages) - 1) & 1))) {
@@ -414,10 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           site = kSitePfVFree;
           break;
         }
-        const int kb = j * BN;
+        const int kb = (sh.j0 + j) * BN;
         const int r0 = it.ctx - kb;                                // first row past the context
         const int r1 = min(BN, ((it.ctx + B - 1) / B) * B - kb);   // end of the last paged block
-        const bool tail = j == sh.n_tiles - 1 && r0 < r1;
+        const bool tail = sh.j0 + j == sh.n_tiles - 1 && r0 < r1;
         const uint32_t vdst = base + kOffV + st * kTile;
         if (lane == 0) {
           const uint32_t land = tail ? bar(BAR_VTAIL) : bar(BAR_VF + st);
@@ -444,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      vc += sh.n_tiles;
+      vc += sh.n;
     }
     if (!ok && lane == 0) raise_error(a.err, kErrTimeout | site);
   } else if (warp == kWarpMma) {
@@ -501,9 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int t = 0; t < sh.nq; ++t) issue_s(t, kc);
         mma_commit(bar(BAR_KE + kc % kKStages));
-        if (sh.n_tiles == 1) mma_commit(bar(BAR_QE));
-        for (int j = 0; ok && j < sh.n_tiles; ++j) {
-          const bool next = j + 1 < sh.n_tiles;
+        if (sh.n == 1) mma_commit(bar(BAR_QE));
+        for (int j = 0; ok && j < sh.n; ++j) {
+          const bool next = j + 1 < sh.n;
           const uint32_t gv = vc + j, gk = kc + j + 1;
           if (!mbar_wait(bar(BAR_VF + gv % kVStages), (gv / kVStages) & 1)) {
             ok = false;
@@ -529,15 +651,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               issue_s(t, gk);
               if (t == sh.nq - 1) {
                 mma_commit(bar(BAR_KE + gk % kKStages));                       // both read K_{j+1}
-                if (j + 2 == sh.n_tiles) mma_commit(bar(BAR_QE));              // the unit's last S
+                if (j + 2 == sh.n) mma_commit(bar(BAR_QE));                    // the piece's last S
               }
             }
           }
         }
-        kc += sh.n_tiles;
-        vc += sh.n_tiles;
-        cnt0 += sh.n_tiles;
-        if (sh.nq > 1) cnt1 += sh.n_tiles;
+        kc += sh.n;
+        vc += sh.n;
+        cnt0 += sh.n;
+        if (sh.nq > 1) cnt1 += sh.n;
       }
       if (!ok) raise_error(a.err, kErrTimeout | site);
       mma_commit(bar(BAR_DONE));                   // every MMA issued so far has completed
@@ -569,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int limit = min(sh.p + qi, it.ctx - 1);  // last key this row sees
       const int warp_limit = min(sh.p + it.row0 + BM * t + 32 * wq, it.ctx - 1);   // smallest in the warp
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; ok && j < sh.n_tiles; ++j) {
+      for (int j = 0; ok && j < sh.n; ++j) {
         if (!mbar_wait(bar(BAR_S + t), (cnt + j) & 1)) {
           ok = false;
           site = kSitePfS;
@@ -579,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sr[128];
         tmem_ld128(lane_base, sr);
         tmem_wait_ld();
-        const int kb = j * BN;
+        const int kb = (sh.j0 + j) * BN;
         float mt = -INFINITY;
         if (kb + BN - 1 > warp_limit) {            // the tile crosses some row's diagonal: mask
 #pragma unroll
@@ -600,7 +722,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_use = resc ? m_new : m;
         const float alpha = resc ? ex2(m - m_new) : 1.0f;
         const uint64_t scale2 = f2_pack(sl2, sl2);
-        const uint64_t neg_m2 = f2_pack(-m_use, -m_use);
+        // a row that sees no key of the segment so far (a later segment's
+        // keys lie past its diagonal) keeps m = -inf and gets p = 0
+        const float m_sub = m_use == -INFINITY ? 0.0f : m_use;
+        const uint64_t neg_m2 = f2_pack(-m_sub, -m_sub);
         uint64_t sum2[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 64; ++c) {             // P packed in place over the scores
@@ -646,31 +771,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(BAR_P + t));
       }
       if (!ok) break;
-      if (!mbar_wait(bar(BAR_O + t), (cnt + sh.n_tiles - 1) & 1)) {
+      if (!mbar_wait(bar(BAR_O + t), (cnt + sh.n - 1) & 1)) {
         ok = false;
         site = kSitePfO;
         break;
       }
       tc_fence_after();
-      const float inv = 1.0f / l;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + (size_t(it.c0 + qi) * H + it.h) * HD;
+      const int e_row = it.c0 + qi, e_h = it.h, e_slot0 = it.slot0, e_j0 = sh.j0, e_ntiles = sh.n_tiles;
+      const bool e_real = qi < it.q_len;
+      __nv_bfloat16* const e_dst = static_cast<__nv_bfloat16*>(a.out) + (size_t(e_row) * H + e_h) * HD;
+      if (e_slot0 < 0) {
+        const float inv = 1.0f / l;
+        __nv_bfloat16* dst = e_dst;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + 128 + 32 * c, o);
-        tmem_wait_ld();
-        if (qi < it.q_len) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + 128 + 32 * c, o);
+          tmem_wait_ld();
+          if (e_real) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float* f = reinterpret_cast<const float*>(&o[8 * e]);
-            d4[e] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
-                               pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+            for (int e = 0; e < 4; ++e) {
+              const float* f = reinterpret_cast<const float*>(&o[8 * e]);
+              d4[e] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                                 pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+            }
           }
         }
+      } else {
+        segment_epilogue(w.partials + size_t(e_slot0) * kSlotFloats + BM * t + i,
+                         w.tickets + (e_slot0 * kSegTicketsPerSlot + t * 4 + wq), (e_ntiles + seg - 1) / seg,
+                         e_j0 / seg, m, l, lane_base + 128, lane, e_dst, e_real);
       }
       tc_fence_before();                           // O read before the next unit's first P V overwrites it
-      cnt += sh.n_tiles;
+      cnt += sh.n;
     }
     if (!ok && lane == 0) raise_error(a.err, kErrTimeout | site);
   }
@@ -731,12 +865,14 @@ cb_status launch_prefill_tc(const AttnArgs& a, const StepPlan& plan, bool after_
   }
   PrefillWork w;
   w.units = plan.pre_units;
+  w.tickets = plan.pre_tickets;
+  w.partials = plan.pre_partials;
   w.header = plan.header;
   w.claims = plan.header + 3;
-  w.unit_cap = plan.pre_cap * a.num_heads;
+  w.unit_cap = plan.pre_cap * a.num_heads + kPrefillSegSlots;
   w.tag = plan.tag;
-  // one CTA per SM, never more than units could exist
-  const int64_t max_units = int64_t(plan.pre_cap) * a.num_heads;
+  // one CTA per SM, never more than entries could exist
+  const int64_t max_units = int64_t(plan.pre_cap) * a.num_heads + kPrefillSegSlots;
   const int64_t grid = std::min<int64_t>(sm_count(), max_units);
   if (grid < 1) return CB_OK;
   cudaError_t e = launch_kernel(prefill_tc_kernel, dim3(unsigned(grid)), dim3(kThreads), kSmemBytes, stream,

@@ -63,21 +63,29 @@ def test_workspace_size_rules(native_lib):
 
     def bf16_step(S, T, max_ctx, H=32, A=128):
         # header + decode items and their unsorted copy [S*splits] + prefill
-        # chunk records and their unsorted copy [T/256 + min(S, T/2) + 1] +
-        # prefill units [that * H] (int2 each) + tickets [S,H] + partials,
-        # all for the shortest split (512 keys)
+        # chunk records and their unsorted copy [T/256 + min(S, T/2) + 1]
+        # (int2 each) + prefill entries [that * H + 1024] (int4) + segment
+        # tickets [1024, 8] + segment partials [1024, A+2, 256] fp32 (a prefill
+        # chunk with contexts past 2048 keys only) + tickets [S,H] + split
+        # partials, all for the shortest split (512 keys)
         splits = (max_ctx + 511) // 512
         pre_cap = T // 256 + min(S, T // 2) + 1
+        seg = 1024 * 256 * (A + 2) * 4 if T > S and max_ctx > 2048 else 0
         partials = S * H * splits * (A + 2) * 4 if splits > 1 else 0
-        return (256 + 2 * a256(S * splits * 8) + 2 * a256(pre_cap * 8) + a256(pre_cap * H * 8)
-                + a256(S * H * 4) + partials)
+        return (256 + 2 * a256(S * splits * 8) + 2 * a256(pre_cap * 8) + a256((pre_cap * H + 1024) * 16)
+                + 32768 + seg + a256(S * H * 4) + partials)
 
-    # one split per row: no partials needed
-    assert native_lib.cb_attention_workspace_size(ctypes.byref(c), 8, 8, 512) == bf16_step(8, 8, 512) == 3584
+    # one split per row: no split partials, no segments
+    assert native_lib.cb_attention_workspace_size(ctypes.byref(c), 8, 8, 512) == bf16_step(8, 8, 512) == 54016
     # decode rows with up to 9 splits: partials [S,H,splits,A+2] fp32 dominate
     n = native_lib.cb_attention_workspace_size(ctypes.byref(c), 256, 256, 4097)
-    assert n == bf16_step(256, 256, 4097) == 256 + 36864 + 2560 + 33280 + 32768 + 256 * 32 * 9 * 130 * 4
+    assert n == bf16_step(256, 256, 4097) == (256 + 36864 + 2560 + 82944 + 32768 + 32768
+                                              + 256 * 32 * 9 * 130 * 4)
+    # a prefill chunk over a long context: the segment partials come in
+    n = native_lib.cb_attention_workspace_size(ctypes.byref(c), 1, 2048, 32768)
+    assert n == bf16_step(1, 2048, 32768) > 1024 * 256 * 130 * 4
+    assert native_lib.cb_attention_workspace_size(ctypes.byref(c), 1, 2048, 2048) == bf16_step(1, 2048, 2048)
     c.dtype = native.CB_DTYPE_F32
     c.head_dim = 64
     n = native_lib.cb_attention_workspace_size(ctypes.byref(c), 3, 6, 1024)
-    assert n == 768 + 6 * 32 * 2 * 66 * 4
+    assert n == 768 + 6 * 32 * 2 * 66 * 4   # f32 rows: per-row split partials, no step plan

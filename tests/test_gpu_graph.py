@@ -27,7 +27,8 @@ def _regular(st):
 
 @pytest.mark.parametrize("p,q", [([513, 0, 2000, 77, 1023], [1, 1, 1, 1, 1]),
                                  ([300], [450]),
-                                 ([0, 300, 5, 40, 1000, 2], [600, 1, 77, 1, 129, 257])])
+                                 ([0, 300, 5, 40, 1000, 2], [600, 1, 77, 1, 129, 257]),
+                                 ([6000, 40, 2500], [512, 1, 300])])
 def test_planned_equals_unplanned_bitwise(native_lib, p, q):
     from continuous_batching_ragged_gb300 import api
     from gpu_harness import DeviceStep

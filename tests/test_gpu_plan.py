@@ -3,7 +3,8 @@ that the persistent decode and prefill kernels claim.  A step's output must
 depend only on the step's inputs: never on what the workspace held before the
 call, and never on which CTA claimed which unit.  The batches cover each route
 through cb_ragged_attention (decode only, one prefill chunk alone, mixed) and
-the plan's special cases (exactly one prefill item; several sorted by cost)."""
+the plan's special cases (exactly one prefill item; several sorted by cost;
+query pairs cut into KV segments, whose arrival tickets live in the workspace)."""
 import numpy as np
 import pytest
 import torch
@@ -17,6 +18,7 @@ CASES = {
     "prefill_only": ([300], [450]),
     "mixed_one_prefill_item": ([100, 700, 0, 40], [1, 1, 200, 1]),
     "mixed_sorted_items": ([0, 300, 5, 40, 1000, 2], [600, 1, 77, 1, 129, 257]),
+    "prefill_kv_segments": ([6000, 40, 2500], [512, 1, 300]),
 }
 
 
