@@ -77,7 +77,7 @@ enum : int {
   BAR_QE = 1,                  // every S MMA of the unit has read Q
   BAR_S = 2,                   // + t: S_t ready
   BAR_P = BAR_S + kQTiles,     // + t: P_t written (128 arrivals)
-  BAR_O = BAR_P + kQTiles,     // + t: P_t V done
+  BAR_O = BAR_P + kQTiles,     // + t: the piece's last P_t V done
   BAR_KF = BAR_O + kQTiles,    // + stage: K landed
   BAR_KE = BAR_KF + kKStages,  // + stage: K consumed
   BAR_VF = BAR_KE + kKStages,  // + stage: V landed (and its tail zeroed)
@@ -584,13 +584,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar(BAR_S + t));
       };
-      auto issue_pv = [&](int t, uint32_t g, bool accumulate) {
+      // O_t is signalled once per piece, after its last P V: inside a piece
+      // the softmax needs no O barrier, because the commit behind S_t(j+1)
+      // already covers every earlier MMA of this thread, P_t V_j included.
+      auto issue_pv = [&](int t, uint32_t g, bool accumulate, bool last) {
         const uint32_t vb = base + kOffV + (g % kVStages) * kTile;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
           mma_f16_ts(tmem + 256 * t + 128, tmem + 256 * t + k * 8, smem_desc(vb + k * 2048, kHalf, 1024), idO,
                      accumulate || k > 0);
-        mma_commit(bar(BAR_O + t));
+        if (last) mma_commit(bar(BAR_O + t));
       };
       // Fixed issue order per KV tile j: P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1).
       // S_t(j+1) overwrites the TMEM columns that P_t V_j reads; tcgen05.mma
@@ -639,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            issue_pv(t, gv, j > 0);
+            issue_pv(t, gv, j > 0, !next);
             if (t == sh.nq - 1) mma_commit(bar(BAR_VE + gv % kVStages));        // both read V_j
             if (next) {
               if (t == 0 && !mbar_wait(bar(BAR_KF + gk % kKStages), (gk / kKStages) & 1)) {
@@ -672,7 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = threadIdx.x - BM * t;            // tile row = TMEM lane
     const uint32_t lane_base = tmem + (uint32_t(wq * 32) << 16) + 256 * t;
     const float sl2 = a.scale_log2;
-    uint32_t cnt = 0;                              // S/O phases of this tile consumed
+    uint32_t cnt = 0;                              // S/P phases of this tile consumed
+    uint32_t ocnt = 0;                             // O phases (one per piece with rows in this tile)
     bool ok = true;
     unsigned site = 0;
     for (int n = 0; ok; ++n) {
@@ -744,14 +748,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float rs = ((rs0 + rs1) + (rs2 + rs3)) + ((rs4 + rs5) + (rs6 + rs7));
         l = l * alpha + rs;
         m = m_use;
-        tc_fence_before();
-        if (j > 0) {                               // P_t V of tile j-1 done: O_t stable
-          if (!mbar_wait(bar(BAR_O + t), (cnt + j - 1) & 1)) {
-            ok = false;
-            site = kSitePfO;
-            break;
-          }
-          tc_fence_after();
+        // S_t(j) done implies P_t V_{j-1} done (one thread issues both, in
+        // order, and the commit behind S_t(j) covers all earlier MMAs): O_t
+        // is stable for the rescale, and P_t(j) may overwrite P_t(j-1)
+        if (j > 0) {
           if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -771,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(BAR_P + t));
       }
       if (!ok) break;
-      if (!mbar_wait(bar(BAR_O + t), (cnt + sh.n - 1) & 1)) {
+      if (!mbar_wait(bar(BAR_O + t), ocnt & 1)) {
         ok = false;
         site = kSitePfO;
         break;
@@ -805,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();                           // O read before the next unit's first P V overwrites it
       cnt += sh.n;
+      ++ocnt;
     }
     if (!ok && lane == 0) raise_error(a.err, kErrTimeout | site);
   }
