@@ -257,6 +257,57 @@ __device__ __forceinline__ void tile_update(const float (&qf)[EPV], const uint4 
   m_run = m_new;
 }
 
+// tile_update for the GU query heads of one key/value head, with the same
+// arithmetic per head (so the same bits), but each K and V row converted to
+// fp32 once for all GU heads instead of once per head.
+template <int GU, int EPV, int LPR, int RPL, int NR>
+__device__ __forceinline__ void group_tile_update(const float (&qf)[GU][EPV], const uint4 (&kv)[NR],
+                                                  const uint4 (&vv)[NR], int base, int k1, int lane,
+                                                  float (&m_run)[GU], float (&l_run)[GU], float (&acc)[GU][EPV]) {
+  using T = __nv_bfloat16;
+  const int g = lane / LPR, c = lane % LPR;
+  float sc[GU][NR];
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    float kf[EPV];
+    Vec16<T>::to_float(kv[i], kf);
+#pragma unroll
+    for (int hh = 0; hh < GU; ++hh) {
+      float d = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) d = fmaf(qf[hh][e], kf[e], d);
+      sc[hh][i] = d;
+    }
+  }
+  const int idx = c / (LPR / NR);
+  const int my_row = base + g + RPL * idx;
+  float pr[GU];
+#pragma unroll
+  for (int hh = 0; hh < GU; ++hh) {
+    transpose_reduce<NR, LPR>(sc[hh], lane);
+    const float sv = my_row < k1 ? sc[hh][0] : -INFINITY;
+    const float m_new = fmaxf(m_run[hh], warp_max(sv));
+    const float alpha = ex2(m_run[hh] - m_new);
+    pr[hh] = ex2(sv - m_new);
+    const float psum = warp_sum((c % (LPR / NR)) == 0 ? pr[hh] : 0.f);
+    l_run[hh] = l_run[hh] * alpha + psum;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[hh][e] *= alpha;
+    m_run[hh] = m_new;
+  }
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    float vf[EPV];
+    Vec16<T>::to_float(vv[i], vf);
+#pragma unroll
+    for (int hh = 0; hh < GU; ++hh) {
+      const float pi = __shfl_sync(0xffffffffu, pr[hh], g * LPR + i * (LPR / NR));
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) acc[hh][e] = fmaf(pi, vf[e], acc[hh][e]);
+    }
+  }
+}
+
 template <typename T, int A>
 __device__ __forceinline__ void load_q(const AttnArgs& a, int t, int h, int c, float (&qf)[Vec16<T>::N]) {
   constexpr int EPV = Vec16<T>::N;
@@ -450,7 +501,7 @@ constexpr uint32_t bulk_smem_bytes() {
 // next, so the copies of the next unit are in flight while the current one
 // is merged and written.
 template <int GU>
-__global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const SplitArgs sa) {
+__global__ void __launch_bounds__(kWarps * 32, 2) split_kv_persistent_kernel(const SplitArgs sa) {
   using T = __nv_bfloat16;
   constexpr int A = 128, EPV = 8, LPR = 16, RPL = 2, NR = 8;
   const AttnArgs& a = sa.a;
@@ -623,9 +674,10 @@ __global__ void __launch_bounds__(kWarps * 32) split_kv_persistent_kernel(const 
         kv[i] = in ? *reinterpret_cast<const uint4*>(kt + r * 256 + c * 16) : make_uint4(0, 0, 0, 0);
         vv[i] = in ? *reinterpret_cast<const uint4*>(kt + kTileBytes + r * 256 + c * 16) : make_uint4(0, 0, 0, 0);
       }
-#pragma unroll
-      for (int hh = 0; hh < GU; ++hh)
-        tile_update<T, EPV, LPR, RPL, NR>(qf[hh], kv, vv, base, U0.k1, lane, m_run[hh], l_run[hh], acc[hh]);
+      if (GU == 1)
+        tile_update<T, EPV, LPR, RPL, NR>(qf[0], kv, vv, base, U0.k1, lane, m_run[0], l_run[0], acc[0]);
+      else
+        group_tile_update<GU, EPV, LPR, RPL, NR>(qf, kv, vv, base, U0.k1, lane, m_run, l_run, acc);
       __syncwarp();                         // every lane has used what it read: the slot may be refilled
       ++consumed;
       top_up();
