@@ -257,9 +257,13 @@ __device__ __forceinline__ void tile_update(const float (&qf)[EPV], const uint4 
   m_run = m_new;
 }
 
-// tile_update for the GU query heads of one key/value head, with the same
-// arithmetic per head (so the same bits), but each K and V row converted to
-// fp32 once for all GU heads instead of once per head.
+// tile_update for the GU query heads of one key/value head: each K and V row
+// is converted to fp32 once for all GU heads, and two per-tile reductions go:
+//  * the running max m_run (warp-uniform) moves only when some score of the
+//    tile exceeds it by more than 8 in the exp2 domain (one vote; the warp
+//    max and the rescale run only then), so p stays below 2^8;
+//  * l_run is this lane's partial row sum (each row counted by one lane of
+//    its pair), summed over the warp once per unit, before the merge.
 template <int GU, int EPV, int LPR, int RPL, int NR>
 __device__ __forceinline__ void group_tile_update(const float (&qf)[GU][EPV], const uint4 (&kv)[NR],
                                                   const uint4 (&vv)[NR], int base, int k1, int lane,
@@ -286,14 +290,16 @@ __device__ __forceinline__ void group_tile_update(const float (&qf)[GU][EPV], co
   for (int hh = 0; hh < GU; ++hh) {
     transpose_reduce<NR, LPR>(sc[hh], lane);
     const float sv = my_row < k1 ? sc[hh][0] : -INFINITY;
-    const float m_new = fmaxf(m_run[hh], warp_max(sv));
-    const float alpha = ex2(m_run[hh] - m_new);
-    pr[hh] = ex2(sv - m_new);
-    const float psum = warp_sum((c % (LPR / NR)) == 0 ? pr[hh] : 0.f);
-    l_run[hh] = l_run[hh] * alpha + psum;
+    if (__any_sync(0xffffffffu, sv > m_run[hh] + 8.0f)) {
+      const float m_new = fmaxf(m_run[hh], warp_max(sv));
+      const float alpha = ex2(m_run[hh] - m_new);
+      l_run[hh] *= alpha;
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) acc[hh][e] *= alpha;
-    m_run[hh] = m_new;
+      for (int e = 0; e < EPV; ++e) acc[hh][e] *= alpha;
+      m_run[hh] = m_new;
+    }
+    pr[hh] = ex2(sv - m_run[hh]);
+    if ((c % (LPR / NR)) == 0) l_run[hh] += pr[hh];
   }
 #pragma unroll
   for (int i = 0; i < NR; ++i) {
@@ -681,6 +687,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) split_kv_persistent_kernel(con
       __syncwarp();                         // every lane has used what it read: the slot may be refilled
       ++consumed;
       top_up();
+    }
+    if (GU > 1) {                           // the grouped update keeps per-lane row sums
+#pragma unroll
+      for (int hh = 0; hh < GU; ++hh) l_run[hh] = warp_sum(l_run[hh]);
     }
     finish_group<GU>(sa, U0, m_run, l_run, acc, sm);
     U0 = U1;
