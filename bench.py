@@ -714,7 +714,9 @@ def main():
                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     dom["frac"] = dom["achieved"] / dom["peak"]
     if dom["bound"] == "hbm":
-        prof, alg = "split_kv_persistent_decode_64seq.md", work["decode_bytes"]
+        prof = ("split_kv_persistent_gqa_decode_64seq.md" if b.kv_heads != b.num_heads
+                else "split_kv_persistent_decode_64seq.md")
+        alg = work["decode_bytes"]
     else:
         prof, alg = "prefill_tc_persistent_long_prompt_last_chunk.md", work["prefill_bytes"]
     ratio = profiled_traffic_ratio(prof) if b.dtype == "bf16" else None
