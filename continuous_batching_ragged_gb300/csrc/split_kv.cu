@@ -53,6 +53,21 @@ struct SplitArgs {
   int32_t wait_previous;    // persistent decode: wait for the kernel launched before (the plan)
 };
 
+// Packed fp32 pairs (Blackwell f32x2 FMA): two FMAs per instruction.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -258,7 +273,9 @@ __device__ __forceinline__ void tile_update(const float (&qf)[EPV], const uint4 
 }
 
 // tile_update for the GU query heads of one key/value head: each K and V row
-// is converted to fp32 once for all GU heads, and two per-tile reductions go:
+// is converted to fp32 once for all GU heads, the dot products and P V
+// updates run two lanes of work per packed f32x2 FMA, and two per-tile
+// reductions go:
 //  * the running max m_run (warp-uniform) moves only when some score of the
 //    tile exceeds it by more than 8 in the exp2 domain (one vote; the warp
 //    max and the rescale run only then), so p stays below 2^8;
@@ -277,10 +294,12 @@ __device__ __forceinline__ void group_tile_update(const float (&qf)[GU][EPV], co
     Vec16<T>::to_float(kv[i], kf);
 #pragma unroll
     for (int hh = 0; hh < GU; ++hh) {
-      float d = 0.f;
+      uint64_t d2 = pk2(0.f, 0.f);
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) d = fmaf(qf[hh][e], kf[e], d);
-      sc[hh][i] = d;
+      for (int e = 0; e < EPV; e += 2) d2 = fma2(pk2(qf[hh][e], qf[hh][e + 1]), pk2(kf[e], kf[e + 1]), d2);
+      float d0, d1;
+      unpk2(d2, d0, d1);
+      sc[hh][i] = d0 + d1;
     }
   }
   const int idx = c / (LPR / NR);
@@ -308,8 +327,12 @@ __device__ __forceinline__ void group_tile_update(const float (&qf)[GU][EPV], co
 #pragma unroll
     for (int hh = 0; hh < GU; ++hh) {
       const float pi = __shfl_sync(0xffffffffu, pr[hh], g * LPR + i * (LPR / NR));
+      const uint64_t pi2 = pk2(pi, pi);
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) acc[hh][e] = fmaf(pi, vf[e], acc[hh][e]);
+      for (int e = 0; e < EPV; e += 2) {
+        const uint64_t a2 = fma2(pi2, pk2(vf[e], vf[e + 1]), pk2(acc[hh][e], acc[hh][e + 1]));
+        unpk2(a2, acc[hh][e], acc[hh][e + 1]);
+      }
     }
   }
 }
