@@ -32,14 +32,16 @@ constexpr int kUnitsPerCta = 6;        // decode units per persistent CTA the sp
 constexpr int kRowCache = 2048;        // rows whose (q_len, ctx) stay in shared memory after pass 1
 // Cost model of a mixed step's SM split, fitted on GB300 to the long-prompt
 // chunk and to %globaltimer stamps of the mixed step's two kernels running
-// side by side: a prefill unit costs about 2.75 us plus 1.1 us per (KV tile x
-// query tile) on one SM; decode streams K/V at about 6.5 TB/s overall, and at
+// side by side, then retuned by timing the mixed step over the per-tile cost
+// (0.9 / 1.1 / 1.3 / 1.5 us): a prefill unit costs about 2.75 us plus 1.3 us
+// per (KV tile x query tile) on one SM, the rate of a prefill SM while decode
+// shares the GPU's memory system; decode streams K/V at about 6.5 TB/s overall, and at
 // most at the per-SM rate the host passes (lower when a unit serves several
 // query heads: then the decode kernel is bound by its arithmetic, not by
 // memory).  A split is taken only if it beats the two kernels one after the
 // other (prefill on every SM, then decode) by kSplitGain.
 constexpr float kPrefillUsPerUnit = 2.75f;
-constexpr float kPrefillUsPerCost = 1.1f;
+constexpr float kPrefillUsPerCost = 1.3f;
 constexpr float kDecodeBytesPerUs = 6.5e6f;
 constexpr float kSplitGain = 0.9f;
 // Prefill KV segments: a query pair's keys are cut into segments of L KV
