@@ -429,7 +429,7 @@ def launches_per_layer(st):
 
 
 def trace_step_roofline(step, num_layers, num_heads, head_dim, peaks):
-    """Roofline time of one step over all layers (SURVEY.md-style algorithmic bytes/flops)."""
+    """Roofline time of one step over all layers (algorithmic bytes and flops)."""
     e = 2
     H, A = num_heads, head_dim
     ctx = step["ctx"].astype(np.int64)

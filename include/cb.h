@@ -203,7 +203,7 @@ cb_status cb_ragged_attention_planned(const void* q, const cb_kv_cache* cache,
 
 /* ---------------------------------------------------------------------------
  * cb_decode_attention_noalloc -- decode attention that allocates nothing.
- * The paper has no counterpart: this is a deployment variant of the decode
+ * The sources have no counterpart: this is a deployment variant of the decode
  * rows of cb_ragged_attention for callers that cannot allocate device memory
  * and have no workspace to lend -- for example an op running inside a host
  * framework whose caching allocator (or a KV pool sized to fill the GPU)

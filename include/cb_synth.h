@@ -3,7 +3,7 @@
  *
  * Not part of the attention step: tests and benchmarks use these to create
  * workloads too large to build on the host (a decode step over ~10 GB of
- * cached keys and values).  The paper has no counterpart; the values follow a
+ * cached keys and values).  The sources describe no such generator; the values follow a
  * published counter-based generator so that a host implementation can
  * recompute any element independently:
  *
