@@ -574,13 +574,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);   // Q (K-major) x K (K-major)
       constexpr uint32_t idO = idesc_bf16_f32(BM, HD, true);    // P (TMEM) x V (N-contiguous)
+      // Shared-memory descriptors built once: a descriptor's address field is
+      // the byte address / 16 (14 bits, and every address here is below
+      // 256 KB), so moving to another tile, stage or K step adds the offset
+      // / 16 to the descriptor itself.
+      const uint64_t dq0 = smem_desc(base + kOffQ, 16, 1024);
+      const uint64_t dk0 = smem_desc(base + kOffK, 16, 1024);
+      const uint64_t dv0 = smem_desc(base + kOffV, kHalf, 1024);
       auto issue_s = [&](int t, uint32_t g) {
-        const uint32_t kb = base + kOffK + (g % kKStages) * kTile;
-        const uint32_t qb = base + kOffQ + t * kTile;
+        const uint64_t kd = dk0 + (((g % kKStages) * kTile) >> 4);
+        const uint64_t qd = dq0 + ((t * kTile) >> 4);
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
-          const uint32_t off = (k / 4) * kHalf + (k % 4) * 32;
-          mma_f16_ss(tmem + 256 * t, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024), idS, k > 0);
+          const uint32_t off16 = ((k / 4) * kHalf + (k % 4) * 32) >> 4;
+          mma_f16_ss(tmem + 256 * t, qd + off16, kd + off16, idS, k > 0);
         }
         mma_commit(bar(BAR_S + t));
       };
@@ -588,11 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the softmax needs no O barrier, because the commit behind S_t(j+1)
       // already covers every earlier MMA of this thread, P_t V_j included.
       auto issue_pv = [&](int t, uint32_t g, bool accumulate, bool last) {
-        const uint32_t vb = base + kOffV + (g % kVStages) * kTile;
+        const uint64_t vd = dv0 + (((g % kVStages) * kTile) >> 4);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          mma_f16_ts(tmem + 256 * t + 128, tmem + 256 * t + k * 8, smem_desc(vb + k * 2048, kHalf, 1024), idO,
-                     accumulate || k > 0);
+          mma_f16_ts(tmem + 256 * t + 128, tmem + 256 * t + k * 8, vd + ((k * 2048) >> 4), idO, accumulate || k > 0);
         if (last) mma_commit(bar(BAR_O + t));
       };
       // Fixed issue order per KV tile j: P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1).
