@@ -110,8 +110,11 @@ cb_status cb_append_kv(const void* k_new, const void* v_new, const int64_t* slot
  *                 flags (CB_ERR_INVALID) and skips any sequence exceeding them.
  *   out           device [num_tokens][H][A] of cache->dtype; every row written.
  *   workspace     device scratch of at least cb_attention_workspace_size(...)
- *                 bytes, 256-byte aligned, used by split-KV decoding; its
- *                 contents need no initialisation and are not preserved.
+ *                 bytes, 256-byte aligned: the step's work lists, split-KV
+ *                 decode partials, and (bf16, when num_tokens > num_seqs and
+ *                 max_context_len > 2048) 136 MB of partial rows for prefill
+ *                 pairs cut into KV segments; its contents need no
+ *                 initialisation and are not preserved.
  *   Concurrent calls must not share one workspace.
  * Built combinations: bf16 with head_dim 128 and block_size in {8,16,32,64,128}
  * (prefill chunks on tcgen05 tensor cores, decode rows split-KV on CUDA cores);
