@@ -149,16 +149,22 @@ def cb_append_kv_dims(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: to
 
 def cb_plan_step(cache: KVCache, cu_seqlens_q: torch.Tensor, context_lens: torch.Tensor, *,
                  num_tokens: int, max_blocks_per_seq: int, max_q_len: int, max_context_len: int,
-                 workspace: torch.Tensor, dims: Optional[torch.Tensor] = None, stream=None) -> None:
-    """Build the step's work lists in `workspace` (sizes are capacities when dims is given)."""
+                 workspace: torch.Tensor, dims: Optional[torch.Tensor] = None,
+                 num_q_heads: Optional[int] = None, stream=None) -> None:
+    """Build the step's work lists in `workspace` (sizes are capacities when dims is given).
+    num_q_heads: query heads of the planned calls when they differ from the
+    cache's (grouped-query attention, cb_plan_step_gqa)."""
     for name, t in (("cu_seqlens_q", cu_seqlens_q), ("context_lens", context_lens)):
         if t.dtype != torch.int32:
             raise ValueError(f"{name} must be int32")
     c = cache.c_struct()
-    check(native.lib().cb_plan_step(
-        ctypes.byref(c), _ptr(cu_seqlens_q), _ptr(context_lens), _ptr(dims), context_lens.shape[0],
-        num_tokens, max_blocks_per_seq, max_q_len, max_context_len, _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream_handle(stream)), "cb_plan_step")
+    rest = (_ptr(cu_seqlens_q), _ptr(context_lens), _ptr(dims), context_lens.shape[0], num_tokens,
+            max_blocks_per_seq, max_q_len, max_context_len, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if num_q_heads is None:
+        check(native.lib().cb_plan_step(ctypes.byref(c), *rest), "cb_plan_step")
+    else:
+        check(native.lib().cb_plan_step_gqa(ctypes.byref(c), num_q_heads, *rest), "cb_plan_step_gqa")
 
 
 def cb_ragged_attention_planned(q: torch.Tensor, cache: KVCache, cu_seqlens_q: torch.Tensor,
@@ -166,13 +172,18 @@ def cb_ragged_attention_planned(q: torch.Tensor, cache: KVCache, cu_seqlens_q: t
                                 max_q_len: int, max_context_len: int, scale: float, out: torch.Tensor,
                                 workspace: torch.Tensor, dims: Optional[torch.Tensor] = None,
                                 stream=None) -> torch.Tensor:
-    """cb_ragged_attention over the plan cb_plan_step built in `workspace`."""
+    """cb_ragged_attention over the plan cb_plan_step built in `workspace`.  When
+    q has more heads than the cache (grouped-query attention) the call goes to
+    cb_ragged_attention_planned_gqa, over a plan made with the same num_q_heads."""
     c = cache.c_struct()
-    check(native.lib().cb_ragged_attention_planned(
-        _ptr(q), ctypes.byref(c), _ptr(cu_seqlens_q), _ptr(context_lens), _ptr(block_tables), _ptr(dims),
-        context_lens.shape[0], q.shape[0], block_tables.shape[1], max_q_len, max_context_len, float(scale),
-        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream)),
-        "cb_ragged_attention_planned")
+    rest = (ctypes.byref(c), _ptr(cu_seqlens_q), _ptr(context_lens), _ptr(block_tables), _ptr(dims),
+            context_lens.shape[0], q.shape[0], block_tables.shape[1], max_q_len, max_context_len, float(scale),
+            _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if q.shape[1] == cache.num_heads:
+        check(native.lib().cb_ragged_attention_planned(_ptr(q), *rest), "cb_ragged_attention_planned")
+    else:
+        check(native.lib().cb_ragged_attention_planned_gqa(_ptr(q), q.shape[1], *rest),
+              "cb_ragged_attention_planned_gqa")
     return out
 
 

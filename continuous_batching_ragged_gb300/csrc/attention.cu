@@ -132,7 +132,7 @@ struct PlanRecord {
   cb::StepPlan plan;
   const int32_t *cu, *ctx, *dims;
   int32_t num_seqs, num_tokens, max_blocks_per_seq, max_q_len, max_context_len;
-  int32_t num_heads, head_dim, block_size, num_blocks;
+  int32_t num_q_heads, num_heads, head_dim, block_size, num_blocks;
   size_t workspace_bytes;
 };
 std::mutex g_plans_mutex;
@@ -207,23 +207,25 @@ extern "C" cb_status cb_ragged_attention_gqa(const void* q, int32_t num_q_heads,
                    workspace_bytes, stream);
 }
 
-extern "C" cb_status cb_plan_step(const cb_kv_cache* cache, const int32_t* cu_seqlens_q,
-                                  const int32_t* context_lens, const int32_t* dims, int32_t num_seqs,
-                                  int32_t num_tokens, int32_t max_blocks_per_seq, int32_t max_q_len,
-                                  int32_t max_context_len, void* workspace, size_t workspace_bytes,
-                                  void* stream) {
-  const char* who = "cb_plan_step";
+namespace {
+
+// cb_plan_step for num_q_heads query heads (a multiple of the cache's heads).
+cb_status plan_step(const char* who, const cb_kv_cache* cache, int32_t num_q_heads, const int32_t* cu_seqlens_q,
+                    const int32_t* context_lens, const int32_t* dims, int32_t num_seqs, int32_t num_tokens,
+                    int32_t max_blocks_per_seq, int32_t max_q_len, int32_t max_context_len, void* workspace,
+                    size_t workspace_bytes, void* stream) {
   if (!cache) return cb::fail(CB_ERR_INVALID, "%s: null cache", who);
   if (cache->dtype != CB_DTYPE_BF16 || cache->block_size % 16 != 0)
     return cb::fail(CB_ERR_UNSUPPORTED, "%s: planned steps need bf16 and a block size multiple of 16", who);
   // the plan reads only the metadata (q, out, block tables and pools are not needed)
   cb::AttnArgs a;
   cb_status st = prepare(who, nullptr, cache, cu_seqlens_q, context_lens, nullptr, num_seqs, num_tokens,
-                         max_blocks_per_seq, max_q_len, max_context_len, 1.0f, nullptr, dims, true, a);
+                         max_blocks_per_seq, max_q_len, max_context_len, 1.0f, nullptr, dims, true, a,
+                         num_q_heads);
   if (st != CB_OK) return st;
   if (num_seqs == 0) return CB_OK;
   PlanRecord rec;
-  st = cb::step_plan_layout(workspace, workspace_bytes, num_seqs, num_tokens, cache->num_heads, cache->head_dim,
+  st = cb::step_plan_layout(workspace, workspace_bytes, num_seqs, num_tokens, a.num_heads, cache->head_dim,
                             max_context_len, &rec.plan);
   if (st != CB_OK) return st;
   rec.plan.dec_ctas = cb::decode_persistent_ctas(a);
@@ -240,6 +242,7 @@ extern "C" cb_status cb_plan_step(const cb_kv_cache* cache, const int32_t* cu_se
   rec.max_blocks_per_seq = max_blocks_per_seq;
   rec.max_q_len = max_q_len;
   rec.max_context_len = max_context_len;
+  rec.num_q_heads = a.num_heads;
   rec.num_heads = cache->num_heads;
   rec.head_dim = cache->head_dim;
   rec.block_size = cache->block_size;
@@ -250,17 +253,17 @@ extern "C" cb_status cb_plan_step(const cb_kv_cache* cache, const int32_t* cu_se
   return CB_OK;
 }
 
-extern "C" cb_status cb_ragged_attention_planned(const void* q, const cb_kv_cache* cache,
-                                                 const int32_t* cu_seqlens_q, const int32_t* context_lens,
-                                                 const int32_t* block_tables, const int32_t* dims,
-                                                 int32_t num_seqs, int32_t num_tokens,
-                                                 int32_t max_blocks_per_seq, int32_t max_q_len,
-                                                 int32_t max_context_len, float scale, void* out,
-                                                 void* workspace, size_t workspace_bytes, void* stream) {
-  const char* who = "cb_ragged_attention_planned";
+// cb_ragged_attention_planned for num_q_heads query heads.
+cb_status attention_planned(const char* who, const void* q, int32_t num_q_heads, const cb_kv_cache* cache,
+                            const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                            const int32_t* block_tables, const int32_t* dims, int32_t num_seqs,
+                            int32_t num_tokens, int32_t max_blocks_per_seq, int32_t max_q_len,
+                            int32_t max_context_len, float scale, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream) {
   cb::AttnArgs a;
   cb_status st = prepare(who, q, cache, cu_seqlens_q, context_lens, block_tables, num_seqs, num_tokens,
-                         max_blocks_per_seq, max_q_len, max_context_len, scale, out, dims, false, a);
+                         max_blocks_per_seq, max_q_len, max_context_len, scale, out, dims, false, a,
+                         num_q_heads);
   if (st != CB_OK || num_seqs == 0) return st;
   PlanRecord rec;
   {
@@ -271,7 +274,8 @@ extern "C" cb_status cb_ragged_attention_planned(const void* q, const cb_kv_cach
   }
   if (rec.cu != cu_seqlens_q || rec.ctx != context_lens || rec.dims != dims || rec.num_seqs != num_seqs ||
       rec.num_tokens != num_tokens || rec.max_blocks_per_seq != max_blocks_per_seq || rec.max_q_len != max_q_len ||
-      rec.max_context_len != max_context_len || rec.num_heads != cache->num_heads ||
+      rec.max_context_len != max_context_len || rec.num_q_heads != a.num_heads ||
+      rec.num_heads != cache->num_heads ||
       rec.head_dim != cache->head_dim || rec.block_size != cache->block_size ||
       rec.num_blocks != cache->num_blocks || rec.workspace_bytes != workspace_bytes)
     return cb::fail(CB_ERR_INVALID, "%s: the workspace's plan was made for other metadata, sizes or cache shape",
@@ -281,4 +285,51 @@ extern "C" cb_status cb_ragged_attention_planned(const void* q, const cb_kv_cach
   cudaError_t e = cudaMemsetAsync(rec.plan.header + 2, 0, 2 * sizeof(int32_t), main);
   if (e != cudaSuccess) return cb::cuda_fail(e, "clearing the claim counters");
   return run_both(a, rec.plan, false, main);
+}
+
+}  // namespace
+
+extern "C" cb_status cb_plan_step(const cb_kv_cache* cache, const int32_t* cu_seqlens_q,
+                                  const int32_t* context_lens, const int32_t* dims, int32_t num_seqs,
+                                  int32_t num_tokens, int32_t max_blocks_per_seq, int32_t max_q_len,
+                                  int32_t max_context_len, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  return plan_step("cb_plan_step", cache, 0, cu_seqlens_q, context_lens, dims, num_seqs, num_tokens,
+                   max_blocks_per_seq, max_q_len, max_context_len, workspace, workspace_bytes, stream);
+}
+
+extern "C" cb_status cb_plan_step_gqa(const cb_kv_cache* cache, int32_t num_q_heads,
+                                      const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                      const int32_t* dims, int32_t num_seqs, int32_t num_tokens,
+                                      int32_t max_blocks_per_seq, int32_t max_q_len, int32_t max_context_len,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_q_heads < 1) return cb::fail(CB_ERR_INVALID, "cb_plan_step_gqa: num_q_heads < 1");
+  return plan_step("cb_plan_step_gqa", cache, num_q_heads, cu_seqlens_q, context_lens, dims, num_seqs,
+                   num_tokens, max_blocks_per_seq, max_q_len, max_context_len, workspace, workspace_bytes,
+                   stream);
+}
+
+extern "C" cb_status cb_ragged_attention_planned(const void* q, const cb_kv_cache* cache,
+                                                 const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                                 const int32_t* block_tables, const int32_t* dims,
+                                                 int32_t num_seqs, int32_t num_tokens,
+                                                 int32_t max_blocks_per_seq, int32_t max_q_len,
+                                                 int32_t max_context_len, float scale, void* out,
+                                                 void* workspace, size_t workspace_bytes, void* stream) {
+  return attention_planned("cb_ragged_attention_planned", q, 0, cache, cu_seqlens_q, context_lens, block_tables,
+                           dims, num_seqs, num_tokens, max_blocks_per_seq, max_q_len, max_context_len, scale,
+                           out, workspace, workspace_bytes, stream);
+}
+
+extern "C" cb_status cb_ragged_attention_planned_gqa(const void* q, int32_t num_q_heads,
+                                                     const cb_kv_cache* cache, const int32_t* cu_seqlens_q,
+                                                     const int32_t* context_lens, const int32_t* block_tables,
+                                                     const int32_t* dims, int32_t num_seqs, int32_t num_tokens,
+                                                     int32_t max_blocks_per_seq, int32_t max_q_len,
+                                                     int32_t max_context_len, float scale, void* out,
+                                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_q_heads < 1) return cb::fail(CB_ERR_INVALID, "cb_ragged_attention_planned_gqa: num_q_heads < 1");
+  return attention_planned("cb_ragged_attention_planned_gqa", q, num_q_heads, cache, cu_seqlens_q, context_lens,
+                           block_tables, dims, num_seqs, num_tokens, max_blocks_per_seq, max_q_len,
+                           max_context_len, scale, out, workspace, workspace_bytes, stream);
 }

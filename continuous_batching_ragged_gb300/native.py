@@ -21,6 +21,7 @@ NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024      # CB_NOALLOC_SCRATCH_BYTES in cb.h
 EXPORTS = ("cb_append_kv", "cb_attention_workspace_size", "cb_ragged_attention",
            "cb_append_kv_dims", "cb_plan_step", "cb_ragged_attention_planned",
            "cb_ragged_attention_gqa", "cb_attention_workspace_size_gqa",
+           "cb_plan_step_gqa", "cb_ragged_attention_planned_gqa",
            "cb_decode_attention_noalloc",
            "cb_scheduler_create", "cb_scheduler_destroy", "cb_add_request", "cb_build_batch",
            "cb_complete_step", "cb_scheduler_stats", "cb_check_device_errors", "cb_last_error",
@@ -91,6 +92,9 @@ def lib() -> ctypes.CDLL:
         "cb_plan_step": (st, [pcache, vp, vp, vp, i32, i32, i32, i32, i32, vp, sz, vp]),
         "cb_ragged_attention_planned": (st, [vp, pcache, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp,
                                              sz, vp]),
+        "cb_plan_step_gqa": (st, [pcache, i32, vp, vp, vp, i32, i32, i32, i32, i32, vp, sz, vp]),
+        "cb_ragged_attention_planned_gqa": (st, [vp, i32, pcache, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
+                                                 vp, vp, sz, vp]),
         "cb_decode_attention_noalloc": (st, [vp, pcache, vp, vp, vp, i32, i32, i32, i32, f32, vp, vp]),
         "cb_scheduler_create": (st, [ctypes.POINTER(cb_sched_config), ctypes.POINTER(vp)]),
         "cb_scheduler_destroy": (None, [vp]),

@@ -204,6 +204,25 @@ cb_status cb_ragged_attention_planned(const void* q, const cb_kv_cache* cache,
                                       int32_t max_context_len, float scale, void* out,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same two calls for grouped-query attention: q and out carry num_q_heads
+ * heads (a positive multiple of the cache's heads), as in
+ * cb_ragged_attention_gqa; the workspace is sized by
+ * cb_attention_workspace_size_gqa.  A plan made by cb_plan_step_gqa serves
+ * only cb_ragged_attention_planned_gqa calls with the same num_q_heads
+ * (CB_ERR_INVALID otherwise). */
+cb_status cb_plan_step_gqa(const cb_kv_cache* cache, int32_t num_q_heads, const int32_t* cu_seqlens_q,
+                           const int32_t* context_lens, const int32_t* dims, int32_t num_seqs,
+                           int32_t num_tokens, int32_t max_blocks_per_seq, int32_t max_q_len,
+                           int32_t max_context_len, void* workspace, size_t workspace_bytes,
+                           void* stream);
+cb_status cb_ragged_attention_planned_gqa(const void* q, int32_t num_q_heads, const cb_kv_cache* cache,
+                                          const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                          const int32_t* block_tables, const int32_t* dims,
+                                          int32_t num_seqs, int32_t num_tokens,
+                                          int32_t max_blocks_per_seq, int32_t max_q_len,
+                                          int32_t max_context_len, float scale, void* out,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------
  * cb_decode_attention_noalloc -- decode attention that allocates nothing.
  * The sources have no counterpart: this is a deployment variant of the decode

@@ -57,3 +57,48 @@ def test_gqa_head_groups_do_not_leak(native_lib):
     api.cb_check_device_errors()
     changed = [not torch.equal(st.out[:, h].view(torch.int16), base[:, h].view(torch.int16)) for h in range(H)]
     assert changed == [h // (H // Hkv) == 0 for h in range(H)]
+
+
+@pytest.mark.parametrize("H,Hkv", [(8, 2), (32, 8)])
+def test_gqa_planned_equals_unplanned_bitwise(native_lib, H, Hkv):
+    """One grouped-query plan (cb_plan_step_gqa) serves every layer of a step
+    and gives the bits of cb_ragged_attention_gqa, decode rows, prefill
+    chunks and a chunk cut into KV segments included."""
+    from continuous_batching_ragged_gb300 import api
+    from gpu_harness import DeviceStep
+    p, q = [513, 0, 2000, 77, 6000, 300], [1, 129, 1, 1, 300, 40]
+    layers = [DeviceStep(W.make_batch(p, q, num_heads=H, head_dim=128, block_size=16, dtype="bf16",
+                                      seed=230, layer=layer, num_kv_heads=Hkv)) for layer in range(2)]
+    ref = []
+    for st in layers:
+        st.append()
+        st.attend()
+        ref.append(st.out.clone())
+    api.cb_check_device_errors()
+    st0 = layers[0]
+    b = st0.b
+    api.cb_plan_step(st0.cache, st0.cu, st0.ctx, num_tokens=b.T, max_blocks_per_seq=b.block_tables.shape[1],
+                     max_q_len=b.max_q_len, max_context_len=b.max_context_len, workspace=st0.ws, num_q_heads=H)
+    for st in layers:
+        st.out.zero_()
+        api.cb_ragged_attention_planned(st.q, st.cache, st0.cu, st0.ctx, st0.bt, max_q_len=b.max_q_len,
+                                        max_context_len=b.max_context_len, scale=st.scale, out=st.out,
+                                        workspace=st0.ws)
+    api.cb_check_device_errors()
+    for st, r in zip(layers, ref):
+        assert torch.equal(st.out.view(torch.int16), r.view(torch.int16))
+
+
+def test_gqa_plan_refuses_other_head_counts(native_lib):
+    """A plan made for one number of query heads serves no call with another."""
+    from continuous_batching_ragged_gb300 import api, native
+    from gpu_harness import DeviceStep
+    st = DeviceStep(W.make_batch([40, 0], [1, 50], num_heads=8, head_dim=128, block_size=16, dtype="bf16",
+                                 seed=231, num_kv_heads=2))
+    b = st.b
+    api.cb_plan_step(st.cache, st.cu, st.ctx, num_tokens=b.T, max_blocks_per_seq=b.block_tables.shape[1],
+                     max_q_len=b.max_q_len, max_context_len=b.max_context_len, workspace=st.ws, num_q_heads=4)
+    with pytest.raises(native.CBError, match="other metadata"):
+        api.cb_ragged_attention_planned(st.q, st.cache, st.cu, st.ctx, st.bt, max_q_len=b.max_q_len,
+                                        max_context_len=b.max_context_len, scale=st.scale, out=st.out,
+                                        workspace=st.ws)
