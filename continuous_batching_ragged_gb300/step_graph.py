@@ -30,6 +30,8 @@ class StepGraph:
     q, k_new, v_new: one [max_tokens, H, A] tensor per layer; the caller fills
     their first T rows before each replay.  outs: one [max_tokens, H, A]
     tensor per layer (or a single shared one) that receives each layer's rows.
+    q and outs may carry more heads than the caches (grouped-query attention:
+    a multiple of them); k_new and v_new carry the caches' heads.
     """
 
     def __init__(self, caches: List[api.KVCache], q: List[torch.Tensor], k_new: List[torch.Tensor],
@@ -44,6 +46,8 @@ class StepGraph:
         self.max_blocks = max_blocks_per_seq
         self.max_context = max_blocks_per_seq * caches[0].block_size
         self.scale = scale
+        self.num_q_heads = q[0].shape[1]
+        self.grouped = self.num_q_heads != caches[0].num_heads
         S, W = max_seqs, max_blocks_per_seq
         # int32 metadata, one buffer: dims[4] | cu[S+1] | context_lens[S] | block_tables[S*W]
         n = 4 + (S + 1) + S + S * W
@@ -55,7 +59,8 @@ class StepGraph:
         self.dims, self.cu, self.ctx = (self._meta_dev[o[i]:o[i + 1]] for i in range(3))
         self.block_tables = self._meta_dev[o[3]:o[4]].view(S, W)
         self._hv = [self._meta_host.numpy()[o[i]:o[i + 1]] for i in range(4)]
-        ws = api.cb_attention_workspace_size(caches[0], S, self.max_tokens, self.max_context)
+        ws = (api.cb_attention_workspace_size_gqa(caches[0], self.num_q_heads, S, self.max_tokens, self.max_context)
+              if self.grouped else api.cb_attention_workspace_size(caches[0], S, self.max_tokens, self.max_context))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device="cuda")
         self.graph: Optional[torch.cuda.CUDAGraph] = None
         self.num_tokens = 0
@@ -82,7 +87,8 @@ class StepGraph:
     def _step(self) -> None:
         kw = dict(num_tokens=self.max_tokens, max_blocks_per_seq=self.max_blocks,
                   max_q_len=self.max_tokens, max_context_len=self.max_context)
-        api.cb_plan_step(self.caches[0], self.cu, self.ctx, workspace=self.workspace, dims=self.dims, **kw)
+        api.cb_plan_step(self.caches[0], self.cu, self.ctx, workspace=self.workspace, dims=self.dims,
+                         num_q_heads=self.num_q_heads if self.grouped else None, **kw)
         for layer, cache in enumerate(self.caches):
             api.cb_append_kv_dims(self.k_new[layer], self.v_new[layer], self._slots_dev, self.dims, cache)
             api.cb_ragged_attention_planned(

@@ -133,3 +133,56 @@ def test_captured_step_replays_a_trace_bitwise(native_lib):
     for e, g in zip(eager, graphed):
         assert torch.equal(e.k.view(torch.int16), g.k.view(torch.int16))
         assert torch.equal(e.v.view(torch.int16), g.v.view(torch.int16))
+
+
+def test_captured_grouped_query_step_equals_eager_bitwise(native_lib):
+    """A 2-layer step of 8 query / 2 key-value heads captured once and replayed
+    with the metadata of three different steps (decode rows, prefill chunks, a
+    chunk long enough to be cut into KV segments) gives the eager grouped
+    calls' bits."""
+    from continuous_batching_ragged_gb300 import api
+    from continuous_batching_ragged_gb300.step_graph import StepGraph
+    from gpu_harness import DeviceStep
+    Hq, Hkv, layers, cap_tokens, cap_seqs = 8, 2, 2, 1024, 8
+    steps = [([513, 0, 2000, 77], [1, 129, 1, 1]), ([6000, 40, 300], [300, 1, 200]), ([10, 20, 30], [1, 1, 1])]
+    batches = [[W.make_batch(p, q, num_heads=Hq, head_dim=128, block_size=16, dtype="bf16", seed=240 + i,
+                             layer=layer, num_kv_heads=Hkv) for layer in range(layers)]
+               for i, (p, q) in enumerate(steps)]
+    max_blocks = max(b.block_tables.shape[1] for bs in batches for b in bs)
+    num_blocks = max(b.num_blocks for bs in batches for b in bs)
+    scale = 1 / math.sqrt(A)
+    caches = [api.KVCache.empty(num_blocks, Hkv, B, A) for _ in range(layers)]
+    gq = [torch.zeros((cap_tokens, Hq, A), dtype=torch.bfloat16, device="cuda") for _ in range(layers)]
+    gk = [torch.zeros((cap_tokens, Hkv, A), dtype=torch.bfloat16, device="cuda") for _ in range(layers)]
+    gv = [torch.zeros((cap_tokens, Hkv, A), dtype=torch.bfloat16, device="cuda") for _ in range(layers)]
+    go = [torch.zeros((cap_tokens, Hq, A), dtype=torch.bfloat16, device="cuda") for _ in range(layers)]
+    sg = StepGraph(caches, gq, gk, gv, go, max_seqs=cap_seqs, max_blocks_per_seq=max_blocks, scale=scale)
+    for i, bs in enumerate(batches):
+        eager = [DeviceStep(b) for b in bs]          # its own cache, filled with the batch's history
+        ref = []
+        for st in eager:
+            st.append()
+            st.attend()
+            ref.append(st.out.clone())
+        api.cb_check_device_errors()
+        b = bs[0]
+        T = b.T
+        for layer, st in enumerate(eager):          # the graph's caches start from the same history
+            caches[layer].k.zero_()
+            caches[layer].v.zero_()
+            caches[layer].k[:st.cache.k.shape[0]].copy_(st.cache.k)
+            caches[layer].v[:st.cache.v.shape[0]].copy_(st.cache.v)
+            gq[layer][:T].copy_(st.q)
+            gk[layer][:T].copy_(st.k_new)
+            gv[layer][:T].copy_(st.v_new)
+        bt = np.full((b.num_seqs, max_blocks), -1, dtype=np.int32)
+        bt[:, :b.block_tables.shape[1]] = b.block_tables
+        sg.load(b.cu_seqlens_q, b.context_lens, bt, b.slot_mapping, b.max_q_len, b.max_context_len)
+        if sg.graph is None:
+            sg.run_eager()
+            torch.cuda.synchronize()
+            sg.capture()
+        sg.replay()
+        api.cb_check_device_errors()
+        for layer in range(layers):
+            assert torch.equal(go[layer][:T].view(torch.int16), ref[layer].view(torch.int16)), (i, layer)
