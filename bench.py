@@ -260,7 +260,7 @@ def time_oracle(b, budget_s: float):
 
 def run_trace_graph(torch, api, W, requests, *, num_layers, num_heads, head_dim, block_size,
                     token_budget, num_blocks, seed, max_steps=100000, admission="reserve_lifetime",
-                    stats_out=None):
+                    stats_out=None, num_kv_heads=None):
     """run_trace with each step captured once as a CUDA graph (StepGraph):
     per step the host builds the batch, the device generator writes every
     layer's Q/K/V (not timed), the metadata is copied into the graph's fixed
@@ -268,14 +268,16 @@ def run_trace_graph(torch, api, W, requests, *, num_layers, num_heads, head_dim,
     cb_append_kv_dims + cb_ragged_attention_planned for every layer."""
     from continuous_batching_ragged_gb300.step_graph import StepGraph
     dt = torch.bfloat16
-    caches = [api.KVCache.empty(num_blocks, num_heads, block_size, head_dim, dt) for _ in range(num_layers)]
+    hkv = num_kv_heads or num_heads
+    caches = [api.KVCache.empty(num_blocks, hkv, block_size, head_dim, dt) for _ in range(num_layers)]
     for c in caches:
         c.k.zero_()
         c.v.zero_()
     longest = max(r.prompt_len + r.output_len for r in requests)
     max_blocks = (longest + block_size - 1) // block_size + 1
-    shape = (token_budget, num_heads, head_dim)
-    q, k, v = ([torch.zeros(shape, dtype=dt, device="cuda") for _ in range(num_layers)] for _ in range(3))
+    shape, kv_shape = (token_budget, num_heads, head_dim), (token_budget, hkv, head_dim)
+    q = [torch.zeros(shape, dtype=dt, device="cuda") for _ in range(num_layers)]
+    k, v = ([torch.zeros(kv_shape, dtype=dt, device="cuda") for _ in range(num_layers)] for _ in range(2))
     out = [torch.zeros(shape, dtype=dt, device="cuda")]
     sg = StepGraph(caches, q, k, v, out, max_seqs=token_budget, max_blocks_per_seq=max_blocks,
                    scale=1.0 / math.sqrt(head_dim))
@@ -331,14 +333,16 @@ def run_trace_graph(torch, api, W, requests, *, num_layers, num_heads, head_dim,
 
 def run_trace(torch, api, W, requests, *, num_layers, num_heads, head_dim, block_size,
               token_budget, num_blocks, seed, on_layer=None, max_steps=100000,
-              admission="reserve_lifetime", stats_out=None):
+              admission="reserve_lifetime", stats_out=None, num_kv_heads=None):
     """Serve ``requests`` to completion.  Each step: cb_build_batch on the host,
     metadata to the device, then per layer the step's Q/K/V (device generator,
     keyed by request id and position, not timed) followed by the timed
     cb_append_kv + cb_ragged_attention on that layer's cache.  Returns per-step
     records (tokens, host scheduler seconds, device attention milliseconds)."""
     dt = torch.bfloat16
-    caches = [api.KVCache.empty(num_blocks, num_heads, block_size, head_dim, dt)
+    hkv = num_kv_heads or num_heads
+    grouped = hkv != num_heads
+    caches = [api.KVCache.empty(num_blocks, hkv, block_size, head_dim, dt)
               for _ in range(num_layers)]
     for c in caches:
         c.k.zero_()
@@ -373,12 +377,14 @@ def run_trace(torch, api, W, requests, *, num_layers, num_heads, head_dim, block
         ctx = torch.from_numpy(bt.context_lens).cuda()
         btab = torch.from_numpy(bt.block_tables).cuda()
         slots = torch.from_numpy(bt.slot_mapping).cuda()
-        need = api.cb_attention_workspace_size(caches[0], S, T, bt.max_context_len)
+        need = (api.cb_attention_workspace_size_gqa(caches[0], num_heads, S, T, bt.max_context_len) if grouped
+                else api.cb_attention_workspace_size(caches[0], S, T, bt.max_context_len))
         if need > ws.numel():
             ws = torch.empty(need, dtype=torch.uint8, device="cuda")
         if qkv is None or qkv[0].shape[0] < T:
-            qkv = [torch.empty((max(T, token_budget), num_heads, head_dim), dtype=dt, device="cuda")
-                   for _ in range(4)]
+            rows_cap = max(T, token_budget)
+            qkv = [torch.empty((rows_cap, h, head_dim), dtype=dt, device="cuda")
+                   for h in (num_heads, hkv, hkv, num_heads)]
         q, k, v, out = (t[:T] for t in qkv)
         events = []
         for layer in range(num_layers):
@@ -387,9 +393,9 @@ def run_trace(torch, api, W, requests, *, num_layers, num_heads, head_dim, block
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             api.cb_append_kv(k, v, slots, caches[layer])
-            api.cb_ragged_attention(q, caches[layer], cu, ctx, btab, max_q_len=bt.max_q_len,
-                                    max_context_len=bt.max_context_len, scale=scale, out=out,
-                                    workspace=ws)
+            attend = api.cb_ragged_attention_gqa if grouped else api.cb_ragged_attention
+            attend(q, caches[layer], cu, ctx, btab, max_q_len=bt.max_q_len,
+                   max_context_len=bt.max_context_len, scale=scale, out=out, workspace=ws)
             e1.record(stream)
             events.append((e0, e1))
             if on_layer is not None:       # runs in stream order, before the next layer reuses `out`
@@ -428,14 +434,16 @@ def launches_per_layer(st):
     return 1 + attention_launches(st["S"], st["T"], st["max_q_len"])
 
 
-def trace_step_roofline(step, num_layers, num_heads, head_dim, peaks):
-    """Roofline time of one step over all layers (algorithmic bytes and flops)."""
+def trace_step_roofline(step, num_layers, num_heads, head_dim, peaks, num_kv_heads=None):
+    """Roofline time of one step over all layers (algorithmic bytes and flops):
+    each cached K/V byte once, q and out, the append; flops over query heads."""
     e = 2
     H, A = num_heads, head_dim
+    Hkv = num_kv_heads or num_heads
     ctx = step["ctx"].astype(np.int64)
     q = step["q_lens"].astype(np.int64)
     p = ctx - q
-    bytes_ = int(ctx.sum()) * 2 * H * A * e + step["T"] * H * A * e * 2 + 4 * step["T"] * H * A * e
+    bytes_ = int(ctx.sum()) * 2 * Hkv * A * e + step["T"] * H * A * e * 2 + 4 * step["T"] * Hkv * A * e
     flops = 4 * A * H * int(np.sum(q * p + q * (q + 1) // 2))
     t = max(bytes_ / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops_sustained"] * 1e12))
     return num_layers * t * 1e3, num_layers * bytes_, num_layers * flops
@@ -503,9 +511,12 @@ def run_trace_bench(args, graph=False):
     cfg = dict(W.SERVING_TRACE)
     if args.trace_blocks:
         cfg["num_blocks"] = args.trace_blocks
+    cfg["num_kv_heads"] = args.kv_heads or cfg["num_heads"]
     reqs = W.serving_trace()
     label = (f"serving_trace_{len(reqs)}req_{cfg['num_layers']}layers_m{cfg['token_budget']}_"
-             f"{cfg['num_blocks']}blocks_bf16_H32_A128_B16")
+             f"{cfg['num_blocks']}blocks_bf16_H{cfg['num_heads']}_A128_B16")
+    if cfg["num_kv_heads"] != cfg["num_heads"]:
+        label += f"_Hkv{cfg['num_kv_heads']}"
     if args.admission != "reserve_lifetime":
         label += "_" + args.admission
     rank, world, local = dist_info()
@@ -522,6 +533,7 @@ def run_trace_bench(args, graph=False):
             batch = o.build_batch()
             o.complete_step()
         b = W.RaggedBatch(num_heads=cfg["num_heads"], head_dim=cfg["head_dim"],
+                          num_kv_heads=cfg["num_kv_heads"],
                           block_size=cfg["block_size"], dtype="bf16", seed=4, layer=0,
                           seq_ids=batch.request_ids, p=(batch.context_lens - batch.q_lens).astype(np.int64),
                           q_len=batch.q_lens.astype(np.int64), block_tables=batch.block_tables,
@@ -536,7 +548,7 @@ def run_trace_bench(args, graph=False):
     peaks = load_peaks()
     kw = dict(num_layers=cfg["num_layers"], num_heads=cfg["num_heads"], head_dim=cfg["head_dim"],
               block_size=cfg["block_size"], token_budget=cfg["token_budget"],
-              num_blocks=cfg["num_blocks"], seed=4)
+              num_blocks=cfg["num_blocks"], seed=4, num_kv_heads=cfg["num_kv_heads"])
     runner = run_trace_graph if graph else run_trace
     kw["admission"] = args.admission
     # warm-up: a short trace of the first requests
@@ -551,8 +563,8 @@ def run_trace_bench(args, graph=False):
     busy = [st for st in steps if st["T"] > 0]
     tokens = sum(st["T"] for st in busy)
     gpu_ms = sum(st["gpu_ms"] for st in busy)
-    roof = [trace_step_roofline(st, cfg["num_layers"], cfg["num_heads"], cfg["head_dim"], peaks)
-            for st in busy]
+    roof = [trace_step_roofline(st, cfg["num_layers"], cfg["num_heads"], cfg["head_dim"], peaks,
+                                cfg["num_kv_heads"]) for st in busy]
     fracs = np.array([r[0] / st["gpu_ms"] for r, st in zip(roof, busy)])
     sched_us = 1e6 * np.mean([st["sched_s"] for st in steps])
     line = {"metric": METRIC, "value": tokens / (gpu_ms * 1e-3), "unit": UNIT, "n_gpus": 1,
@@ -560,7 +572,10 @@ def run_trace_bench(args, graph=False):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": label, "requests": len(reqs), "layers": cfg["num_layers"],
-                       "tokens_total": tokens, "l2": "inputs larger than L2 (86 GB of KV pools)",
+                       "tokens_total": tokens,
+                       "l2": "inputs larger than L2 (%.0f GB of KV pools)" % (
+                           cfg["num_blocks"] * cfg["block_size"] * cfg["num_kv_heads"] * cfg["head_dim"] * 2 * 2
+                           * cfg["num_layers"] / 1e9),
                        "timed": "cb_append_kv + cb_ragged_attention of every layer of every step; "
                                 "Q/K/V generation between layers not timed"},
             "step_roofline": {"frac_total": sum(r[0] for r in roof) / gpu_ms,
@@ -598,6 +613,8 @@ def main():
     ap.add_argument("--admission", default="reserve_lifetime", choices=["reserve_lifetime", "prompt_preempt"],
                     help="scheduler admission policy of the trace workloads")
     ap.add_argument("--trace-blocks", type=int, default=0, help="KV pool blocks of the trace workloads")
+    ap.add_argument("--kv-heads", type=int, default=0,
+                    help="key/value heads of the trace workloads (grouped-query attention; 0: one per query head)")
     ap.add_argument("--decode-seqs", type=int, default=256,
                     help="sequences of the decode workload (smaller cases for profiling)")
     args = ap.parse_args()
