@@ -38,6 +38,10 @@
 //     forms exp arguments and row sums two at a time with packed f32x2
 //     FMA/add, writes P as bf16 into TMEM, and at the end normalises O and
 //     stores its row.
+// When a step has few, long query pairs, the plan cuts a pair's key range
+// into KV segments that run as separate pieces: each stores its unnormalised
+// rows in a partial slot, and the last to finish merges them (log-sum-exp,
+// in slot order).
 // Every wait is bounded; a timeout sets the device error word and the CTA
 // winds down, freeing its TMEM.
 #include <algorithm>
@@ -307,7 +311,7 @@ __device__ __forceinline__ void grid_dependency_wait() {
 struct PrefillWork {
   const int4* units;        // the plan's entries (sequence, pair | head << 16, j0 | j1 << 16, slot0)
   int32_t* tickets;         // arrival counters of segmented pairs: [slot0][query tile * 4 + warp]
-  float* partials;          // [slot][256 rows][HD + 2] segment results (acc, max, sum)
+  float* partials;          // [slot][HD + 2][256 rows] segment results (acc, max, sum), dimension-major
   const int32_t* header;    // [1] = number of units
   int32_t* claims;          // claim counter
   int32_t unit_cap;         // capacity of the unit list
