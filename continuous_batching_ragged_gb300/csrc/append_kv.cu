@@ -1,8 +1,8 @@
 // K1: append this step's keys and values to the block-paged cache.
 //
 // Page "continuous-batching" (zhangchitc.github.io), section "Inside the
-// kernel": the new keys and values are written into the KV cache, each into
-// its own request's entry, before attention reads the cache back.
+// kernel": a step first stores every new key and value row under the request
+// it belongs to; attention then reads the cache.
 //
 // A pure copy, HBM-bound.  A token's K (and V) rows are contiguous in k_new;
 // a (token, head) row of head_dim * elem bytes lands contiguously at

@@ -105,8 +105,10 @@ extern "C" cb_status cb_decode_attention_noalloc(const void* q, const cb_kv_cach
   a.scale_log2 = scale * 1.4426950408889634f;
   a.dtype = cache->dtype;
   a.err = err;
-  // The split tickets must start at zero: launch_split_kv clears them on the
-  // stream before the kernel (cudaMemsetAsync, no allocation).
+  // The split tickets and claim counters must start at zero, whatever the
+  // previous call left in the array: the step-plan kernel that launch_split_kv
+  // runs first zeroes them, on the same stream, before the decode kernel
+  // reads them.
   return cb::launch_split_kv(a, false, scratch, size_t(CB_NOALLOC_SCRATCH_BYTES),
                              static_cast<cudaStream_t>(stream));
 }

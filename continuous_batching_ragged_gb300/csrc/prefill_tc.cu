@@ -45,6 +45,7 @@
 // Every wait is bounded; a timeout sets the device error word and the CTA
 // winds down, freeing its TMEM.
 #include <algorithm>
+#include <mutex>
 
 #include <cuda.h>
 
@@ -828,6 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+std::mutex g_attr_mutex;
 bool g_attr_set[64] = {};
 
 }  // namespace
@@ -868,11 +870,14 @@ cb_status launch_prefill_tc(const AttnArgs& a, const StepPlan& plan, bool after_
   }
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kSmemBytes));
-    if (e != cudaSuccess) return cuda_fail(e, "prefill chunks: shared memory attribute");
-    g_attr_set[dev] = true;
+  if (dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(g_attr_mutex);   // first calls may race from several host threads
+    if (!g_attr_set[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(kSmemBytes));
+      if (e != cudaSuccess) return cuda_fail(e, "prefill chunks: shared memory attribute");
+      g_attr_set[dev] = true;
+    }
   }
   PrefillWork w;
   w.units = plan.pre_units;

@@ -24,6 +24,7 @@
 //     memory, then across splits by the last CTA of the row to finish (an
 //     atomic ticket), which writes the output row.
 #include <algorithm>
+#include <mutex>
 #include <cfloat>
 
 #include "device_common.cuh"
@@ -766,8 +767,12 @@ float decode_rate_per_sm(int group_heads) {
 
 template <int GU>
 static int persistent_ctas(int dev) {
+  // One-time, per-device set-up; first calls may come from several host
+  // threads at once, so it runs under a lock.
+  static std::mutex mu;
   static int ctas_per_sm[64] = {};
   static bool ready[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
   if (!ready[dev]) {
     cudaError_t e = cudaFuncSetAttribute(split_kv_persistent_kernel<GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(bulk_smem_bytes<GU>()));

@@ -72,8 +72,8 @@ typedef struct {
 /* ---------------------------------------------------------------------------
  * cb_append_kv -- write this step's keys and values into the cache.
  * Page "continuous-batching" (zhangchitc.github.io), section "Inside the
- * kernel": the new keys and values are written into the KV cache, each into
- * its own request's entry, before attention reads the cache back.
+ * kernel": a step first stores every new key and value row under the request
+ * it belongs to; attention then reads the cache.
  *
  *   k_new, v_new  device [num_tokens][num_heads][head_dim] of cache->dtype,
  *                 16-byte aligned.

@@ -1,10 +1,9 @@
 """Block-paged KV cache writes and reads (oracle; test infrastructure only).
 
 Page "continuous-batching" (zhangchitc.github.io), section "Inside the
-kernel: cu_seqlens splits six rows back into three": the step's keys and
-values are first written into the cache, each into its own request's entry;
-then every key and value the request has is read back, block by block, for
-attention.  hassanahmed.net, "How Continuous Batching Speeds Up LLM Serving",
+kernel": a step first stores every new key and value row under the request
+it belongs to; attention then gathers all of that request's keys and values
+from the cache, one block after another.  hassanahmed.net, "How Continuous Batching Speeds Up LLM Serving",
 paragraph on PagedAttention: the cache is stored in fixed-size blocks.
 
 Pool layout: one array per K and V, [num_blocks, H, B, A].  A token with
