@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "ragged-attention step tokens/s on 1 GB300; % HBM / tensor roofline per step"
 UNIT = "tokens/s"
 NOMINAL_HBM_GBS = 8000.0
+L2_FLUSH_BELOW = 512 * 2 ** 20      # steps moving fewer bytes get an L2 flush between timed steps
 
 
 # ---------------------------------------------------------------------------
@@ -167,14 +168,20 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 class Staged:
-    def __init__(self, b, torch, api, W):
+    """One step's inputs in HBM.  With `cache` given, the step runs on that
+    cache as it stands (its cached prefix is not regenerated)."""
+
+    def __init__(self, b, torch, api, W, cache=None):
         dt = torch.bfloat16 if b.dtype == "bf16" else torch.float32
         self.b = b
-        self.cache = api.KVCache.empty(b.num_blocks, b.kv_heads, b.block_size, b.head_dim, dt)
-        self.cache.k.zero_()
-        self.cache.v.zero_()
+        fill = cache is None
+        if cache is None:
+            cache = api.KVCache.empty(b.num_blocks, b.kv_heads, b.block_size, b.head_dim, dt)
+            cache.k.zero_()
+            cache.v.zero_()
+        self.cache = cache
         sid = torch.from_numpy(b.seq_ids).cuda()
-        if int(b.p.max()) > 0:
+        if fill and int(b.p.max()) > 0:
             pl = torch.from_numpy(b.p.astype(np.int32)).cuda()
             bt = torch.from_numpy(b.block_tables).cuda()
             for kind, pool in ((W.KIND_K, self.cache.k), (W.KIND_V, self.cache.v)):
@@ -228,11 +235,12 @@ def _random_inputs(n_max, c_max, H, A, Hkv=None):
     return _RANDOM_CACHE[key]
 
 
-def time_oracle(b, budget_s: float):
+def time_oracle(b, budget_s: float, detail: bool = False):
     """Time the oracle (as it stands) on a bounded sample of the workload's
     sequences, with random inputs of the workload's shapes (drawn once and
     sliced per sequence; drawing them is not timed).  Returns (tokens/s,
-    sample description, cores, seconds spent)."""
+    sample description, cores, seconds spent), plus the query tokens and
+    sequences processed with detail."""
     from oracle import attention as oa
     H, A = b.num_heads, b.head_dim
     scale = 1.0 / math.sqrt(A)
@@ -251,6 +259,8 @@ def time_oracle(b, budget_s: float):
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     sample = (f"{done_seqs} of {b.num_seqs} sequences ({done_tokens} of {b.T} query tokens, all "
               f"{H} heads), fp64 numpy, random inputs of the workload's shapes")
+    if detail:
+        return done_tokens / spent, sample, cores, spent, done_tokens, done_seqs
     return done_tokens / spent, sample, cores, spent
 
 
@@ -260,12 +270,14 @@ def time_oracle(b, budget_s: float):
 
 def run_trace_graph(torch, api, W, requests, *, num_layers, num_heads, head_dim, block_size,
                     token_budget, num_blocks, seed, max_steps=100000, admission="reserve_lifetime",
-                    stats_out=None, num_kv_heads=None):
+                    stats_out=None, num_kv_heads=None, on_step=None, per_layer_outs=False):
     """run_trace with each step captured once as a CUDA graph (StepGraph):
     per step the host builds the batch, the device generator writes every
     layer's Q/K/V (not timed), the metadata is copied into the graph's fixed
     buffers, and the timed region is one graph replay -- the step plan, then
-    cb_append_kv_dims + cb_ragged_attention_planned for every layer."""
+    cb_append_kv_dims + cb_ragged_attention_planned for every layer.
+    per_layer_outs gives every layer its own output buffer (default: one
+    shared buffer); on_step(step, batch, outs) runs after each replay."""
     from continuous_batching_ragged_gb300.step_graph import StepGraph
     dt = torch.bfloat16
     hkv = num_kv_heads or num_heads
@@ -278,7 +290,7 @@ def run_trace_graph(torch, api, W, requests, *, num_layers, num_heads, head_dim,
     shape, kv_shape = (token_budget, num_heads, head_dim), (token_budget, hkv, head_dim)
     q = [torch.zeros(shape, dtype=dt, device="cuda") for _ in range(num_layers)]
     k, v = ([torch.zeros(kv_shape, dtype=dt, device="cuda") for _ in range(num_layers)] for _ in range(2))
-    out = [torch.zeros(shape, dtype=dt, device="cuda")]
+    out = [torch.zeros(shape, dtype=dt, device="cuda") for _ in range(num_layers if per_layer_outs else 1)]
     sg = StepGraph(caches, q, k, v, out, max_seqs=token_budget, max_blocks_per_seq=max_blocks,
                    scale=1.0 / math.sqrt(head_dim))
     sched = api.Scheduler(token_budget, block_size, num_blocks, admission=admission)
@@ -317,6 +329,8 @@ def run_trace_graph(torch, api, W, requests, *, num_layers, num_heads, head_dim,
         e1.record(stream)
         torch.cuda.synchronize()
         api.cb_check_device_errors()
+        if on_step is not None:
+            on_step(step, bt, [o[:T] for o in out])
         t0 = time.perf_counter()
         sched.complete_step()
         t_sched += time.perf_counter() - t0
@@ -480,33 +494,55 @@ def dist_info():
     return rank, world, local
 
 
+def workload_config(b, label, work, world=1):
+    """The `config` object of a step workload's line (the same in both arms)."""
+    useful = b.useful_tokens if b.useful_tokens is not None else b.T
+    return {"workload": label, "num_seqs": b.num_seqs, "tokens_per_step": useful, "computed_query_rows": b.T,
+            "kv_bytes_read": int(work["bytes"] - work["append_bytes"]),
+            "l2": ("inputs larger than L2 (KV cache read per step >> 129 MB)" if work["bytes"] > L2_FLUSH_BELOW
+                   else "L2 flushed between timed steps (a 512 MB write outside the step's events)"),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args, b, label):
+    """The reference arm: the oracle, as it stands, on the host cores.  Each
+    step processes the workload's sequences in order until the step's budget
+    (about 150 s over all steps) is spent; when the budget covers every
+    sequence the step is the whole workload.  value = query tokens processed /
+    seconds spent, ms_per_step = seconds spent per step."""
     rank, world, _ = dist_info()
     if rank != 0:
         return
-    per_step = []
-    tokens, cores = 0, 1
-    sample = ""
-    budget = max(0.2, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    work = algorithmic_work(b)
+    budget = max(0.2, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    spent_steps, tokens_steps, seqs_steps = [], [], []
+    cores, sample = 1, ""
     for i in range(args.warmup + args.steps):
-        tps, sample, cores, spent = time_oracle(b, budget)
+        tps, sample, cores, spent, done_tokens, done_seqs = time_oracle(b, budget, detail=True)
         if i >= args.warmup:
-            per_step.append(tps)
-    value = statistics.median(per_step)
+            spent_steps.append(spent)
+            tokens_steps.append(done_tokens)
+            seqs_steps.append(done_seqs)
+    value = sum(tokens_steps) / sum(spent_steps)
+    whole = min(seqs_steps) == b.num_seqs
+    cfg = workload_config(b, label, work)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": b.T / value * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(spent_steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": label, "num_seqs": b.num_seqs,
-                                            "tokens_per_step": b.T},
+            "data": "synthetic", "config": cfg,
+            "reference_step": ("the whole workload per step" if whole else
+                               f"a bounded sample per step: {min(seqs_steps)}-{max(seqs_steps)} of "
+                               f"{b.num_seqs} sequences; value is the sample's rate"),
+            "sampled_tokens_per_step": statistics.mean(tokens_steps),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def run_trace_bench(args, graph=False):
+def run_trace_bench(args, graph=False, print_line=True):
     """The serving trace end to end: 2000 requests, 32 layers, budget 4096
-    (graph: each step one CUDA-graph replay)."""
+    (graph: each step one CUDA-graph replay).  Returns the line (ours arm)."""
     from continuous_batching_ragged_gb300 import workloads as W
     cfg = dict(W.SERVING_TRACE)
     if args.trace_blocks:
@@ -596,7 +632,264 @@ def run_trace_bench(args, graph=False):
         line["config"]["workload"] = label + "_graph"
         line["config"]["timed"] = ("one CUDA-graph replay per step: the step plan, then cb_append_kv_dims + "
                                    "cb_ragged_attention_planned of every layer; Q/K/V generation not timed")
-    print(json.dumps(line), flush=True)
+    line["roofline"] = {"kernel": "whole step (append + attention, all layers)", "bound": "hbm or tensor per step",
+                        "achieved": None, "peak": None, "unit": None,
+                        "frac": line["step_roofline"]["frac_total"], "traffic": None,
+                        "note": "sum over steps of max(bytes / HBM, flops / sustained bf16) over measured time"}
+    if print_line:
+        print(json.dumps(line), flush=True)
+    return line
+
+
+def dominant_roofline(b, work, attn_ms, peaks):
+    """Roofline of the step's dominant kernel: the larger of the decode rows'
+    HBM time and the prefill chunks' tensor time.  Both kernels run inside the
+    one attention call, so in a mixed step the call's time bounds the dominant
+    kernel's time from above (the fraction is then a lower bound)."""
+    t_dec = work["decode_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_pre = work["prefill_flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_dec >= t_pre:
+        dom = {"kernel": "split_kv_persistent_kernel (decode rows)" if b.dtype == "bf16" else "split_kv_kernel",
+               "bound": "hbm", "achieved": work["decode_bytes"] / (attn_ms * 1e-3) / 1e9,
+               "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        prof = ("split_kv_persistent_gqa_decode_64seq.md" if b.kv_heads != b.num_heads
+                else "split_kv_persistent_decode_64seq.md")
+        alg = work["decode_bytes"]
+    else:
+        dom = {"kernel": "prefill_tc_kernel (prefill chunks)", "bound": "tensor",
+               "achieved": work["prefill_flops"] / (attn_ms * 1e-3) / 1e12,
+               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+        prof, alg = "prefill_tc_persistent_long_prompt_last_chunk.md", work["prefill_bytes"]
+    dom["frac"] = dom["achieved"] / dom["peak"]
+    ratio = profiled_traffic_ratio(prof) if b.dtype == "bf16" else None
+    dom["traffic"] = None if ratio is None else ratio * alg
+    if ratio is not None:
+        dom["traffic_source"] = (f"profiles/{prof}: dram bytes per algorithmic byte of an ncu capture "
+                                 f"({ratio}), times this launch's {alg} algorithmic bytes")
+    dom["peak_source"] = f"of {peaks['source']}"
+    return dom
+
+
+def step_roofline_of(work, ms, append_ms, attn_ms, peaks):
+    t_hbm = work["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = work["flops"] / (peaks["bf16_tflops"] * 1e12)
+    return {"bytes": work["bytes"], "flops": work["flops"], "bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "roofline_ms": max(t_hbm, t_tc) * 1e3, "measured_ms": ms,
+            "frac": max(t_hbm, t_tc) * 1e3 / ms,
+            "frac_vs_nominal_8tbs": (work["bytes"] / (NOMINAL_HBM_GBS * 1e9)) * 1e3 / ms,
+            "append_ms": append_ms, "attention_ms": attn_ms}
+
+
+def time_steps(torch, st, steps, stream, flush_buf=None, barrier=False):
+    """Time `steps` steps (append + attention) with CUDA events on `stream`.
+    Without flush_buf: back to back, ms = (end - start) / steps.  With it:
+    the buffer is rewritten before each step, outside the step's events, and
+    ms = the mean of the steps' own event times.  Returns (ms per step, mean
+    append ms, mean attention ms)."""
+    import torch.distributed as dist
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    if barrier:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(steps):
+        if flush_buf is not None:
+            flush_buf.add_(1)
+        ev[i][0].record(stream)
+        st.append()
+        ev[i][1].record(stream)
+        st.attend()
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        dist.barrier()
+    append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    if flush_buf is None:
+        ms = t_start.elapsed_time(t_end) / steps
+    else:
+        ms = statistics.mean(e[0].elapsed_time(e[2]) for e in ev)
+    return ms, append_ms, attn_ms
+
+
+def measure_config(torch, api, W, b, label, peaks, steps, warmup, world=1, barrier=False, min_seconds=0.0):
+    """Stage one step workload in HBM and time `steps` steps after `warmup`
+    untimed ones (more steps when min_seconds asks for a longer timed region,
+    so that the clock sampler sees it).  Returns (result dict, staged step)."""
+    st = Staged(b, torch, api, W)
+    stream = torch.cuda.current_stream()
+    work = algorithmic_work(b)
+    flush = torch.empty(L2_FLUSH_BELOW // 4, dtype=torch.float32, device="cuda").zero_() \
+        if work["bytes"] < L2_FLUSH_BELOW else None
+    for _ in range(warmup):
+        st.append()
+        st.attend()
+    api.cb_check_device_errors()
+    torch.cuda.synchronize()
+    if min_seconds > 0:
+        est, _, _ = time_steps(torch, st, 3, stream, flush)
+        steps = max(steps, int(math.ceil(min_seconds / (est * 1e-3))))
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    ms, append_ms, attn_ms = time_steps(torch, st, steps, stream, flush, barrier)
+    clocks = sampler.stop()
+    api.cb_check_device_errors()
+    cfg = workload_config(b, label, work, world)
+    useful = cfg["tokens_per_step"]
+    res = {"config": cfg, "steps": steps, "ms_per_step": ms, "tokens_per_s": useful / (ms * 1e-3),
+           "roofline": dominant_roofline(b, work, attn_ms, peaks),
+           "step_roofline": step_roofline_of(work, ms, append_ms, attn_ms, peaks),
+           "clocks": clocks,
+           "gpu_launches": (1 + attention_launches(b.num_seqs, b.T, b.max_q_len, b.dtype)) * steps}
+    return res, st
+
+
+def measure_e2e(torch, api, st, steps, world):
+    """The same step through the public API with host buffers: pinned H2D of
+    the step's inputs and metadata, the two calls, D2H of the output."""
+    stream = torch.cuda.current_stream()
+    host = {name: getattr(st, name).cpu().pin_memory() for name in
+            ("q", "k_new", "v_new", "cu", "ctx", "bt", "slots")}
+    dev_in = {name: torch.empty_like(getattr(st, name)) for name in host}
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for name, t in host.items():
+            dev_in[name].copy_(t, non_blocking=True)
+        st.append(k=dev_in["k_new"], v=dev_in["v_new"], slots=dev_in["slots"])
+        st.attend(q=dev_in["q"], cu=dev_in["cu"], ctx=dev_in["ctx"], bt=dev_in["bt"])
+        out_host.copy_(st.out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / steps)
+    api.cb_check_device_errors()
+    useful = st.b.useful_tokens if st.b.useful_tokens is not None else st.b.T
+    return {"value": replica_throughput(useful, e2e_ms, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+
+def oracle_one_thread(workload, decode_seqs, budget):
+    """The oracle timed with one BLAS/OpenMP thread, in a child process (the
+    thread count of numpy's BLAS is fixed when it loads)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, bench; b, _ = bench.make_workload(%r, %d); "
+            "tps, sample, cores, spent = bench.time_oracle(b, %f); "
+            "print(json.dumps([tps, sample]))" % (workload, decode_seqs, budget))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                           timeout=120)
+        tps, sample = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:            # a baseline only: never fail the bench over it
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+    return {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+            "threads": "OMP/OPENBLAS/MKL_NUM_THREADS=1"}
+
+
+def measure_long_prompt(torch, api, W, peaks, steps, warmup):
+    """The long-prompt config as specified: one 32768-token prompt processed in
+    16 chunks of 2048, each appended to the one paged cache and attended over
+    it in turn.  A step is all 16 chunks; tokens/s counts the prompt's tokens."""
+    chunks = [W.long_prompt_chunk(k) for k in range(16)]
+    b0 = chunks[0]
+    cache = api.KVCache.empty(b0.num_blocks, b0.kv_heads, b0.block_size, b0.head_dim, torch.bfloat16)
+    cache.k.zero_()
+    cache.v.zero_()
+    staged = [Staged(b, torch, api, W, cache=cache) for b in chunks]
+    stream = torch.cuda.current_stream()
+    works = [algorithmic_work(b) for b in chunks]
+
+    def one_prompt(ev=None):
+        for i, st in enumerate(staged):
+            if ev is not None:
+                ev[i][0].record(stream)
+            st.append()
+            if ev is not None:
+                ev[i][1].record(stream)
+            st.attend()
+            if ev is not None:
+                ev[i][2].record(stream)
+
+    for _ in range(warmup):
+        one_prompt()
+    api.cb_check_device_errors()
+    torch.cuda.synchronize()
+    evs = [[tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in staged] for _ in range(steps)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        one_prompt(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    api.cb_check_device_errors()
+    ms = t0.elapsed_time(t1) / steps
+    attn_ms = sum(statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for ev in evs) for i in range(16))
+    append_ms = sum(statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for ev in evs) for i in range(16))
+    flops = sum(w["prefill_flops"] for w in works)
+    bytes_ = sum(w["bytes"] for w in works)
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    ratio = profiled_traffic_ratio("prefill_tc_persistent_long_prompt_last_chunk.md")
+    del staged, cache
+    torch.cuda.empty_cache()
+    return {"config": {"workload": "long_prompt_32768_in_16_chunks_of_2048_bf16_H32_A128_B16",
+                       "tokens_per_step": 32768, "chunks": 16,
+                       "l2": "inputs larger than L2 (each chunk reads up to 537 MB of KV)"},
+            "steps": steps, "ms_per_step": ms, "tokens_per_s": 32768 / (ms * 1e-3),
+            "roofline": {"kernel": "prefill_tc_kernel (16 launches, one per chunk)", "bound": "tensor",
+                         "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops"],
+                         "frac_vs_sustained": achieved / peaks["bf16_tflops_sustained"],
+                         "traffic": None if ratio is None else ratio * sum(w["prefill_bytes"] for w in works),
+                         "peak_source": f"of {peaks['source']}"},
+            "step_roofline": {"flops": flops, "bytes": bytes_, "roofline_ms": max(t_tc, t_hbm) * 1e3,
+                              "measured_ms": ms, "frac": max(t_tc, t_hbm) * 1e3 / ms,
+                              "append_ms": append_ms, "attention_ms": attn_ms},
+            "clocks": clocks, "gpu_launches": 16 * 3 * steps}
+
+
+def measure_per_config(torch, api, W, peaks, args):
+    """Every other config, each timed in its own region with its own clock
+    samples: the tiny fp32 step, the mixed step, the long prompt (last chunk
+    alone and all 16 chunks), and the serving trace (eager and graph)."""
+    out = {}
+    warm = max(3, args.warmup)
+    for name in ("tiny", "mixed", "long"):
+        b, label = make_workload(name)
+        res, st = measure_config(torch, api, W, b, label, peaks, max(10, min(args.steps, 100)), warm,
+                                 min_seconds=0.5)
+        del st
+        torch.cuda.empty_cache()
+        out[label] = res
+    res = measure_long_prompt(torch, api, W, peaks, max(5, min(args.steps, 30)), warm)
+    out[res["config"]["workload"]] = res
+    for graph in (False, True):
+        line = run_trace_bench(argparse.Namespace(**dict(vars(args), impl="ours", kv_heads=0, trace_blocks=0,
+                                                         admission="reserve_lifetime")),
+                               graph=graph, print_line=False)
+        keep = ("steps", "ms_per_step", "config", "roofline", "step_roofline", "clocks", "gpu_launches",
+                "gpu_ms_total", "wall_s", "scheduler_us_per_step", "mean_decode_per_step")
+        res = {k: line[k] for k in keep}
+        res["tokens_per_s"] = line["value"]
+        out[line["config"]["workload"]] = res
+    return out
 
 
 def main():
@@ -610,6 +903,8 @@ def main():
                                                              "insertion_padded"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="default workload only: skip the other configs (mixed, long prompt, trace)")
     ap.add_argument("--admission", default="reserve_lifetime", choices=["reserve_lifetime", "prompt_preempt"],
                     help="scheduler admission policy of the trace workloads")
     ap.add_argument("--trace-blocks", type=int, default=0, help="KV pool blocks of the trace workloads")
@@ -640,136 +935,38 @@ def main():
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
-    dev_index = torch.cuda.current_device()
-
-    st = Staged(b, torch, api, W)
-    stream = torch.cuda.current_stream()
-    work = algorithmic_work(b)
     peaks = load_peaks()
 
-    # warm-up (also checks the device error word once)
-    for _ in range(args.warmup):
-        st.append()
-        st.attend()
-    api.cb_check_device_errors()
-    torch.cuda.synchronize()
-
-    launches_per_step = 1 + attention_launches(b.num_seqs, b.T, b.max_q_len, b.dtype)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    sampler = ClockSampler(dev_index)
-    sampler.start()
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        st.append()
-        ev[i][1].record(stream)
-        st.attend()
-        ev[i][2].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-    api.cb_check_device_errors()
-    total_ms = t_start.elapsed_time(t_end)
-    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    ms = total_ms / args.steps
-    ms = max_over_ranks(ms)
-    useful = b.useful_tokens if b.useful_tokens is not None else b.T
+    res, st = measure_config(torch, api, W, b, label, peaks, args.steps, args.warmup, world=world,
+                             barrier=world > 1)
+    ms = max_over_ranks(res["ms_per_step"])
+    useful = res["config"]["tokens_per_step"]
     value = replica_throughput(useful, ms, world)
+    e2e = measure_e2e(torch, api, st, max(10, args.steps // 3), world)
 
-    # end to end through the public API with host buffers: pinned H2D of the
-    # step's inputs and metadata, the two calls, D2H of the output
-    host = {name: getattr(st, name).cpu().pin_memory() for name in
-            ("q", "k_new", "v_new", "cu", "ctx", "bt", "slots")}
-    dev_in = {name: torch.empty_like(getattr(st, name)) for name in host}
-    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
-    e2e_steps = max(10, args.steps // 3)
-
-    def e2e_step():
-        for name, t in host.items():
-            dev_in[name].copy_(t, non_blocking=True)
-        st.append(k=dev_in["k_new"], v=dev_in["v_new"], slots=dev_in["slots"])
-        st.attend(q=dev_in["q"], cu=dev_in["cu"], ctx=dev_in["ctx"], bt=dev_in["bt"])
-        out_host.copy_(st.out, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
-    api.cb_check_device_errors()
-
-    # roofline of the dominant kernel and of the whole step
-    # dominant kernel: the larger of the decode rows' HBM time and the prefill
-    # chunks' tensor time (both kernels run inside the one attention call, so
-    # in a mixed step the call time bounds the dominant kernel's time from above)
-    t_dec = work["decode_bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_pre = work["prefill_flops"] / (peaks["bf16_tflops"] * 1e12)
-    if t_dec >= t_pre:
-        dom = {"kernel": "split_kv_persistent_kernel (decode rows)" if b.dtype == "bf16" else "split_kv_kernel",
-               "bound": "hbm", "achieved": work["decode_bytes"] / (attn_ms * 1e-3) / 1e9,
-               "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        dom = {"kernel": "prefill_tc_kernel (prefill chunks)", "bound": "tensor",
-               "achieved": work["prefill_flops"] / (attn_ms * 1e-3) / 1e12,
-               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    dom["frac"] = dom["achieved"] / dom["peak"]
-    if dom["bound"] == "hbm":
-        prof = ("split_kv_persistent_gqa_decode_64seq.md" if b.kv_heads != b.num_heads
-                else "split_kv_persistent_decode_64seq.md")
-        alg = work["decode_bytes"]
-    else:
-        prof, alg = "prefill_tc_persistent_long_prompt_last_chunk.md", work["prefill_bytes"]
-    ratio = profiled_traffic_ratio(prof) if b.dtype == "bf16" else None
-    dom["traffic"] = None if ratio is None else ratio * alg
-    if ratio is not None:
-        dom["traffic_source"] = (f"profiles/{prof}: dram bytes per algorithmic byte of an ncu capture "
-                                 f"({ratio}), times this launch's {alg} algorithmic bytes")
-    dom["peak_source"] = f"of {peaks['source']}"
-    t_hbm = work["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_tc = work["flops"] / (peaks["bf16_tflops"] * 1e12)
-    step_roof = {"bytes": work["bytes"], "flops": work["flops"],
-                 "bound": "hbm" if t_hbm >= t_tc else "tensor",
-                 "roofline_ms": max(t_hbm, t_tc) * 1e3, "measured_ms": ms,
-                 "frac": max(t_hbm, t_tc) * 1e3 / ms,
-                 "frac_vs_nominal_8tbs": (work["bytes"] / (NOMINAL_HBM_GBS * 1e9)) * 1e3 / ms,
-                 "append_ms": append_ms, "attention_ms": attn_ms}
-
-    cpu = None
+    cpu = cpu_1t = None
     if rank == 0 and not args.no_cpu_baseline:
         tps, sample, cores, _ = time_oracle(b, args.cpu_budget)
         cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        if args.workload in ("decode", "tiny"):
+            cpu_1t = oracle_one_thread(args.workload, args.decode_seqs, min(8.0, args.cpu_budget))
+    del st
+    torch.cuda.empty_cache()
+
+    per_config = None
+    if args.workload == "decode" and world == 1 and not args.no_per_config:
+        per_config = measure_per_config(torch, api, W, peaks, args)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": b.dtype, "data": "synthetic",
-                "config": {"workload": label, "num_seqs": b.num_seqs, "tokens_per_step": useful,
-                           "computed_query_rows": b.T,
-                           "kv_bytes_read": int(work["bytes"] - work["append_bytes"]),
-                           "l2": "inputs larger than L2 (KV cache read per step >> 129 MB)"
-                           if work["bytes"] > 1e9 else "inputs smaller than L2; no flush",
-                           "parallelism": "replicas" if world > 1 else "single GPU"},
-                "roofline": dom, "step_roofline": step_roof, "cpu_baseline": cpu,
-                "e2e": {"value": replica_throughput(useful, e2e_ms, world), "unit": UNIT,
-                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-                "clocks": clocks, "gpu_launches": launches_per_step * args.steps}
+                "config": res["config"], "roofline": res["roofline"], "step_roofline": res["step_roofline"],
+                "cpu_baseline": cpu, "e2e": e2e, "clocks": res["clocks"], "gpu_launches": res["gpu_launches"]}
+        if cpu_1t is not None:
+            line["cpu_baseline_1thread"] = cpu_1t
+        if per_config is not None:
+            line["per_config"] = per_config
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

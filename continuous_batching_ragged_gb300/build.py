@@ -20,6 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcb.so")
+VALUES_SRC = os.path.join(PKG, "hostgen", "token_values.c")
+VALUES_LIB = os.path.join(PKG, "libcb_values.so")
 
 CUDA_SOURCES = ["runtime.cu", "append_kv.cu", "plan.cu", "split_kv.cu", "prefill_tc.cu", "attention.cu",
                 "synth.cu", "decode_noalloc.cu", "selftest.cu"]
@@ -90,5 +92,25 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_values_lib(force: bool = False, verbose: bool = False) -> str:
+    """Compile (if its source changed) the host-only input generator
+    ``libcb_values.so`` with gcc and return its path.  It is separate from
+    libcb.so and shares no source with it."""
+    stamp = VALUES_LIB + ".fingerprint"
+    h = hashlib.sha256(open(VALUES_SRC, "rb").read())
+    h.update(__file__.encode())
+    fp = h.hexdigest()
+    if not force and os.path.exists(VALUES_LIB) and os.path.exists(stamp) and open(stamp).read() == fp:
+        return VALUES_LIB
+    tmp = VALUES_LIB + ".tmp"
+    _run(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", "-o", tmp, VALUES_SRC, "-lm"],
+         verbose)
+    os.replace(tmp, VALUES_LIB)
+    with open(stamp, "w") as f:
+        f.write(fp)
+    return VALUES_LIB
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True))
+    print(build_values_lib(force="--force" in sys.argv, verbose=True))

@@ -104,10 +104,78 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
     return out.view(np.float32).reshape(np.shape(x))
 
 
+_VALUES_LIB = None        # ctypes handle of libcb_values.so, False once it failed to build or load
+
+
+def _values_lib():
+    """The compiled host generator (hostgen/token_values.c), built on first use;
+    None where no C compiler is available (token_values then runs in numpy)."""
+    global _VALUES_LIB
+    if _VALUES_LIB is None:
+        try:
+            import ctypes
+            from . import build as _build
+            lib = ctypes.CDLL(_build.build_values_lib())
+            f = lib.cbv_token_values
+            f.restype = None
+            f.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                          ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32,
+                          ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
+            _VALUES_LIB = lib
+        except Exception:          # no compiler or loader: fall back to numpy
+            _VALUES_LIB = False
+    return _VALUES_LIB or None
+
+
+def _token_values_c(lib, seed, kind, layer, seq_id, positions, heads, head_dim, dtype):
+    """token_values through libcb_values.so, positions split over host threads
+    (ctypes releases the GIL for the call)."""
+    import concurrent.futures
+    import os
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64).reshape(-1).astype(np.uint32))
+    hd = np.ascontiguousarray(np.asarray(list(heads), dtype=np.uint32))
+    out = np.empty((len(pos), len(hd), head_dim), dtype=np.float32)
+    if len(pos) == 0 or len(hd) == 0:
+        return out
+    per_pos = len(hd) * head_dim
+    nthreads = max(1, min(len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 1,
+                          (len(pos) * per_pos) // (1 << 16) + 1))
+    bounds = np.linspace(0, len(pos), nthreads + 1).astype(np.int64)
+    bf16 = 1 if dtype == "bf16" else 0
+
+    def run(i):
+        a, b = int(bounds[i]), int(bounds[i + 1])
+        if b > a:
+            lib.cbv_token_values(seed & 0xFFFFFFFFFFFFFFFF, kind & 0xFFFFFFFF, layer & 0xFFFFFFFF,
+                                 seq_id & 0xFFFFFFFF, pos[a:].ctypes.data, b - a, hd.ctypes.data, len(hd),
+                                 head_dim, bf16, out[a:].ctypes.data)
+
+    if nthreads == 1:
+        run(0)
+    else:
+        with concurrent.futures.ThreadPoolExecutor(nthreads) as ex:
+            list(ex.map(run, range(nthreads)))
+    return out
+
+
 def token_values(seed: int, kind: int, layer: int, seq_id: int,
                  positions: np.ndarray, heads: Sequence[int], head_dim: int,
                  dtype: str) -> np.ndarray:
-    """Values of ``kind`` for one sequence: array [len(positions), len(heads), A]."""
+    """Values of ``kind`` for one sequence: array [len(positions), len(heads), A].
+    Runs the compiled host generator when it is available, else numpy; the two
+    are pinned bit for bit to each other."""
+    if dtype not in ("bf16", "f32"):
+        raise ValueError(dtype)
+    lib = _values_lib()
+    if lib is not None:
+        return _token_values_c(lib, seed, kind, layer, seq_id, positions, heads, head_dim, dtype)
+    return token_values_numpy(seed, kind, layer, seq_id, positions, heads, head_dim, dtype)
+
+
+def token_values_numpy(seed: int, kind: int, layer: int, seq_id: int,
+                       positions: np.ndarray, heads: Sequence[int], head_dim: int,
+                       dtype: str) -> np.ndarray:
+    """token_values written out in numpy (the definition above, step by step)."""
     positions = np.asarray(positions, dtype=np.uint32).reshape(-1, 1, 1)
     heads = np.asarray(heads, dtype=np.uint32).reshape(1, -1, 1)
     dims = np.arange(head_dim, dtype=np.uint32).reshape(1, 1, -1)
@@ -144,6 +212,14 @@ class RaggedBatch:
     name: str = ""
     useful_tokens: Optional[int] = None   # of a padded batch: the real query tokens
     num_kv_heads: Optional[int] = None    # key/value heads (grouped-query attention); None = num_heads
+    # (q_shift, k_slope): shaped inputs whose scores rise along the sequence.
+    # Every query gets q_shift * u added and the key at position j gets
+    # k_slope * j * u, u = (1, ..., 1) / sqrt(A), then the sum is rounded to the
+    # dtype; so scale * q . k grows by about scale * q_shift * k_slope per key
+    # and a row's running maximum keeps climbing as keys stream in.  Values of
+    # such a batch exist only on the host (the device generator does not
+    # shape them).
+    drift: Optional[Tuple[float, float]] = None
 
     @property
     def kv_heads(self) -> int:
@@ -197,6 +273,23 @@ class RaggedBatch:
         return 2 if self.dtype == "bf16" else 4
 
     # -- values ------------------------------------------------------------
+    def values(self, kind: int, s: int, positions, heads) -> np.ndarray:
+        """Values of ``kind`` for sequence s at ``positions`` and ``heads``:
+        [len(positions), len(heads), A], fp32 holding dtype values."""
+        x = token_values(self.seed, kind, self.layer, int(self.seq_ids[s]), positions, heads,
+                         self.head_dim, self.dtype)
+        if self.drift is None or kind == KIND_V:
+            return x
+        q_shift, k_slope = self.drift
+        u = np.full(self.head_dim, 1.0 / math.sqrt(self.head_dim), dtype=np.float32)
+        if kind == KIND_Q:
+            add = np.float32(q_shift) * u
+        else:
+            pos = np.asarray(positions, dtype=np.float32).reshape(-1, 1, 1)
+            add = (np.float32(k_slope) * pos) * u
+        y = (x + add).astype(np.float32)
+        return round_to_bf16(y) if self.dtype == "bf16" else y
+
     def packed(self, kind: int) -> np.ndarray:
         """This step's tokens of ``kind`` packed as [T, heads, A] (fp32 holding dtype
         values); queries have num_heads heads, keys and values kv_heads."""
@@ -206,8 +299,7 @@ class RaggedBatch:
         heads = range(nh)
         for s in range(self.num_seqs):
             pos = np.arange(self.p[s], self.p[s] + self.q_len[s])
-            out[cu[s]:cu[s + 1]] = token_values(self.seed, kind, self.layer, int(self.seq_ids[s]),
-                                                pos, heads, self.head_dim, self.dtype)
+            out[cu[s]:cu[s + 1]] = self.values(kind, s, pos, heads)
         return out
 
     def history(self, s: int, kind: int, heads: Optional[Sequence[int]] = None,
@@ -216,8 +308,7 @@ class RaggedBatch:
         if heads is None:
             heads = range(self.heads_of(kind))
         n = int(self.context_lens[s]) if upto is None else int(upto)
-        return token_values(self.seed, kind, self.layer, int(self.seq_ids[s]),
-                            np.arange(n), heads, self.head_dim, self.dtype)
+        return self.values(kind, s, np.arange(n), heads)
 
     def prefilled_pool(self, kind: int, sentinel: float = float("nan")) -> np.ndarray:
         """Host pool [num_blocks, H, B, A] holding every sequence's cached prefix
@@ -259,7 +350,8 @@ def make_batch(p: Sequence[int], q_len: Sequence[int], *, num_heads: int, head_d
                block_size: int, dtype: str, seed: int, layer: int = 0,
                num_blocks: Optional[int] = None, permute: bool = True,
                seq_ids: Optional[Sequence[int]] = None, name: str = "",
-               num_kv_heads: Optional[int] = None) -> RaggedBatch:
+               num_kv_heads: Optional[int] = None,
+               drift: Optional[Tuple[float, float]] = None) -> RaggedBatch:
     p = np.asarray(p, dtype=np.int64)
     q_len = np.asarray(q_len, dtype=np.int64)
     rng = np.random.Generator(np.random.PCG64(seed + 7919))
@@ -269,7 +361,8 @@ def make_batch(p: Sequence[int], q_len: Sequence[int], *, num_heads: int, head_d
     return RaggedBatch(num_heads=num_heads, head_dim=head_dim, block_size=block_size,
                        dtype=dtype, seed=seed, layer=layer,
                        seq_ids=np.asarray(seq_ids, dtype=np.int64), p=p, q_len=q_len,
-                       block_tables=bt, num_blocks=nb, name=name, num_kv_heads=num_kv_heads)
+                       block_tables=bt, num_blocks=nb, name=name, num_kv_heads=num_kv_heads,
+                       drift=drift)
 
 
 def padded_equivalent(b: RaggedBatch) -> RaggedBatch:

@@ -144,11 +144,11 @@ def oracle_rows(b: W.RaggedBatch, s: int, heads=None, rows=None) -> np.ndarray:
     p, n = int(b.p[s]), int(b.q_len[s])
     pos = np.arange(p, p + n) if rows is None else p + np.asarray(rows)
     c = int(b.context_lens[s]) if rows is None else int(p + np.max(rows) + 1)
-    q = W.token_values(b.seed, W.KIND_Q, b.layer, int(b.seq_ids[s]), pos, heads, b.head_dim, b.dtype)
+    q = b.values(W.KIND_Q, s, pos, heads)
     # the key/value head of each query head (one per query head: the oracle then needs no grouping)
     kvh = [h // (b.num_heads // b.kv_heads) for h in heads]
-    k = W.token_values(b.seed, W.KIND_K, b.layer, int(b.seq_ids[s]), np.arange(c), kvh, b.head_dim, b.dtype)
-    v = W.token_values(b.seed, W.KIND_V, b.layer, int(b.seq_ids[s]), np.arange(c), kvh, b.head_dim, b.dtype)
+    k = b.values(W.KIND_K, s, np.arange(c), kvh)
+    v = b.values(W.KIND_V, s, np.arange(c), kvh)
     if rows is None:
         return oa.attend_sequence(q, k, v, p, 1.0 / math.sqrt(b.head_dim))
     # selected rows: row r sees keys 0..p+r; run each as a one-row chunk at its own offset

@@ -28,8 +28,15 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
-    # tokens/s and ms per step describe the same timing
-    assert abs(d["value"] * d["ms_per_step"] * 1e-3 - d["config"]["tokens_per_step"]) < 1e-6 * d["value"]
+    # tokens/s and ms per step describe the same timing; the tiny step fits
+    # its budget, so each timed step is the whole workload
+    assert d["reference_step"] == "the whole workload per step"
+    assert d["sampled_tokens_per_step"] == d["config"]["tokens_per_step"]
+    assert abs(d["value"] * d["ms_per_step"] * 1e-3 - d["sampled_tokens_per_step"]) < 1e-6 * d["value"]
+    # the same config object as the GPU arm's line
+    for key in ("workload", "num_seqs", "tokens_per_step", "computed_query_rows", "kv_bytes_read", "l2",
+                "parallelism"):
+        assert key in d["config"], key
 
 
 def test_fewer_than_three_warmup_steps_are_refused():

@@ -44,20 +44,21 @@ def test_decode_step_scaled_down(native_lib):
     assert_tolerance(got[:, heads], exp)
 
 
-def test_decode_step_full_size_sampled(native_lib):
-    """The full decode step: 256 sequences, contexts U[512, 4096]; every output
-    row checked for finiteness, 96 (sequence, head) rows against the oracle."""
+def test_decode_step_full_size_every_row(native_lib):
+    """The full decode step, in the launch configuration the bench times: 256
+    sequences, contexts U[512, 4096]; every output row checked for finiteness,
+    and every sequence against the oracle on 4 heads (a different 4 per
+    sequence, so all 32 heads are covered)."""
     from gpu_harness import DeviceStep, assert_tolerance, oracle_rows, to_np
     b = W.decode_step()
     st = DeviceStep(b, source="device")
     out = to_np(st.run())
     assert np.all(np.isfinite(out))
     rng = np.random.default_rng(5)
-    seqs = rng.choice(b.num_seqs, 48, replace=False)
     got, exp = [], []
-    for s in seqs:
-        heads = sorted(rng.choice(32, 2, replace=False).tolist())
-        exp.append(oracle_rows(b, int(s), heads))
+    for s in range(b.num_seqs):
+        heads = sorted(rng.choice(32, 4, replace=False).tolist())
+        exp.append(oracle_rows(b, s, heads))
         got.append(out[b.cu_seqlens_q[s]:b.cu_seqlens_q[s] + 1][:, heads])
     assert_tolerance(np.concatenate(got), np.concatenate(exp))
 

@@ -72,9 +72,14 @@ def _synth_layer(api, seed, layer, rows, pos, tensors):
 
 def test_captured_step_replays_a_trace_bitwise(native_lib):
     """A small scheduler-driven trace (2 layers, budget 256): every step is run
-    eagerly on exact-size tensors and by replaying one captured graph."""
+    eagerly on exact-size tensors and by replaying one captured graph; the
+    two agree bit for bit, and sampled replayed rows of every step and layer
+    match the oracle."""
     from continuous_batching_ragged_gb300 import api
     from continuous_batching_ragged_gb300.step_graph import StepGraph
+    from gpu_harness import assert_tolerance, oracle_rows
+    rng = np.random.default_rng(2)
+    samples = []
     seed, layers, budget, num_blocks = 11, 2, 256, 600
     reqs = W.serving_trace(seed=7, num_requests=24, prompt_median=120, prompt_cap=500, out_median=12,
                            out_min=3, out_max=30)
@@ -127,9 +132,24 @@ def test_captured_step_replays_a_trace_bitwise(native_lib):
         api.cb_check_device_errors()
         for layer in range(layers):
             assert torch.equal(go[layer][:T].view(torch.int16), ref[layer].view(torch.int16)), (steps, layer)
+            # the replayed rows themselves against the oracle: one random
+            # sequence per layer and step, up to 4 of its rows, every head
+            s = int(rng.integers(S))
+            q_len, c = int(bt.q_lens[s]), int(bt.context_lens[s])
+            rows = sorted(set(rng.choice(q_len, min(q_len, 3), replace=False).tolist()) | {q_len - 1})
+            got = go[layer][int(bt.cu_seqlens_q[s]) + np.array(rows)].float().cpu().numpy()
+            samples.append((layer, int(bt.request_ids[s]), c, q_len, rows, got))
         sched.complete_step()
         steps += 1
     assert sched.idle and steps > 20
+    got, exp = [], []
+    for layer, rid, c, q_len, rows, g in samples:
+        b1 = W.RaggedBatch(num_heads=H, head_dim=A, block_size=B, dtype="bf16", seed=seed, layer=layer,
+                           seq_ids=np.array([rid]), p=np.array([c - q_len]), q_len=np.array([q_len]),
+                           block_tables=np.zeros((1, 1), np.int32), num_blocks=1)
+        exp.append(oracle_rows(b1, 0, None, rows))
+        got.append(g)
+    assert_tolerance(np.concatenate(got).astype(np.float64), np.concatenate(exp))
     for e, g in zip(eager, graphed):
         assert torch.equal(e.k.view(torch.int16), g.k.view(torch.int16))
         assert torch.equal(e.v.view(torch.int16), g.v.view(torch.int16))
@@ -139,10 +159,10 @@ def test_captured_grouped_query_step_equals_eager_bitwise(native_lib):
     """A 2-layer step of 8 query / 2 key-value heads captured once and replayed
     with the metadata of three different steps (decode rows, prefill chunks, a
     chunk long enough to be cut into KV segments) gives the eager grouped
-    calls' bits."""
+    calls' bits, and every replayed row matches the oracle."""
     from continuous_batching_ragged_gb300 import api
     from continuous_batching_ragged_gb300.step_graph import StepGraph
-    from gpu_harness import DeviceStep
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_packed, to_np
     Hq, Hkv, layers, cap_tokens, cap_seqs = 8, 2, 2, 1024, 8
     steps = [([513, 0, 2000, 77], [1, 129, 1, 1]), ([6000, 40, 300], [300, 1, 200]), ([10, 20, 30], [1, 1, 1])]
     batches = [[W.make_batch(p, q, num_heads=Hq, head_dim=128, block_size=16, dtype="bf16", seed=240 + i,
@@ -186,3 +206,4 @@ def test_captured_grouped_query_step_equals_eager_bitwise(native_lib):
         api.cb_check_device_errors()
         for layer in range(layers):
             assert torch.equal(go[layer][:T].view(torch.int16), ref[layer].view(torch.int16)), (i, layer)
+            assert_tolerance(to_np(go[layer][:T]), oracle_packed(bs[layer]))   # every replayed row

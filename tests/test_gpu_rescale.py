@@ -1,0 +1,111 @@
+"""Online-softmax rescaling forced under oracle parity.
+
+Page "continuous-batching" (zhangchitc.github.io), section "Inside the
+kernel": a request's cache is read block by block and each block's
+contribution is folded into a running state (row maximum, row sum, weighted
+values).  Both kernels keep that running maximum lazily: the prefill kernel
+(and the grouped-query decode kernel) rescale the accumulated row only when a
+new tile's maximum exceeds the kept one by more than 2^8 in the exp2 domain.
+With the workload's N(0,1) inputs that practically never happens after the
+first tile, so these tests shape the inputs (RaggedBatch.drift) so that every
+row's scores climb steadily along the sequence: the kept maximum is overtaken
+again and again, with the accumulated rows still carrying real weight in the
+final result.  A host-side replay of the lazy rule on the same bf16 inputs
+asserts that the rescale branch is taken, before the outputs are compared
+with the fp64 oracle element by element.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from continuous_batching_ragged_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+SL2 = 1.4426950408889634 / math.sqrt(128)   # scale * log2(e) at head_dim 128
+
+
+def _slope(d128: float, q_shift: float = 4.0) -> float:
+    """k_slope that raises scores by about d128 (exp2 units) per 128 keys."""
+    return d128 / (128 * SL2 * q_shift)
+
+
+def lazy_events(b, s, h, tile, warps=1):
+    """Replay the lazy-max rule on sequence s, query head h: for each row, the
+    number of tiles (after the first one it sees) whose maximum exceeds the
+    kept maximum by more than 8.  Tiles of `tile` keys are taken in turn by
+    `warps` streams (the decode kernel interleaves 16-key tiles over 4 warps;
+    each warp keeps its own maximum)."""
+    p, n, c = int(b.p[s]), int(b.q_len[s]), int(b.context_lens[s])
+    q = b.values(W.KIND_Q, s, np.arange(p, p + n), [h])[:, 0].astype(np.float64)
+    k = b.values(W.KIND_K, s, np.arange(c), [h // (b.num_heads // b.kv_heads)])[:, 0].astype(np.float64)
+    z = (q @ k.T) * SL2
+    out = []
+    for i in range(n):
+        lim = p + i + 1
+        ev = 0
+        for w in range(warps):
+            m, first = -np.inf, True
+            for t0 in range(w * tile, lim, warps * tile):
+                mt = z[i, t0:min(t0 + tile, lim)].max()
+                if mt > m + 8:
+                    ev += 0 if first else 1
+                    m = mt
+                first = False
+        out.append(ev)
+    return np.array(out)
+
+
+@pytest.mark.parametrize("d128", [3.0, 12.0])
+def test_prefill_rescale_forced(native_lib, d128):
+    """Whole query pairs (no KV segments: no pair spans more than 16 KV
+    tiles): chunks over cached prefixes of 0 to 1800 tokens, plus decode
+    rows, with scores rising d128 per KV tile."""
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_packed, to_np
+    b = W.make_batch([0, 700, 1500, 1800, 2000, 900], [256, 300, 129, 200, 1, 1], num_heads=4,
+                     head_dim=128, block_size=16, dtype="bf16", seed=230, drift=(4.0, _slope(d128)))
+    for s in (1, 2, 3):
+        ev = lazy_events(b, s, 1, tile=128)
+        assert np.mean(ev > 0) > 0.8, (s, np.mean(ev > 0))
+    st = DeviceStep(b)
+    got = to_np(st.run())
+    assert _header(st.ws)[9] == 0                 # whole pairs
+    assert_tolerance(got, oracle_packed(b))
+
+
+def _header(ws):
+    return ws[:64].view(__import__("torch").int32).tolist()
+
+
+@pytest.mark.parametrize("kv_heads", [4, 2])
+def test_prefill_segments_rescale_forced(native_lib, kv_heads):
+    """Pairs cut into KV segments (16 tiles each), merged by log-sum-exp: every
+    segment restarts its running maximum and overtakes it again; the merge
+    then weighs segments whose maxima differ by hundreds of exp2 units."""
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_packed, to_np
+    b = W.make_batch([6000, 40, 2500, 3000, 0], [512, 1, 300, 1, 129], num_heads=4, head_dim=128,
+                     block_size=16, dtype="bf16", seed=240 + kv_heads, num_kv_heads=kv_heads,
+                     drift=(4.0, _slope(3.0)))
+    ev = lazy_events(b, 0, 2, tile=128)
+    assert np.mean(ev > 0) > 0.9
+    st = DeviceStep(b)
+    got = to_np(st.run())
+    assert _header(st.ws)[9] == 16
+    assert_tolerance(got, oracle_packed(b))
+
+
+@pytest.mark.parametrize("heads,kv_heads", [(8, 2), (8, 4), (12, 4), (8, 8)])
+def test_decode_rescale_forced(native_lib, heads, kv_heads):
+    """Decode rows: the grouped kernel (4, 2 or 3 query heads per unit) keeps a
+    lazy maximum per warp; the one-head kernel rescales every tile.  Contexts
+    from one tile to 4000 keys, several splits per row."""
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_packed, to_np
+    ctx = [17, 33, 100, 800, 1500, 2500, 4000]
+    b = W.make_batch([c - 1 for c in ctx], [1] * len(ctx), num_heads=heads, head_dim=128, block_size=16,
+                     dtype="bf16", seed=250 + heads + kv_heads, num_kv_heads=kv_heads,
+                     drift=(4.0, _slope(4.0)))
+    rows = [lazy_events(b, s, h, tile=16, warps=4)[0] for s in range(3, len(ctx)) for h in range(heads)]
+    assert np.mean(np.array(rows) > 0) > 0.8
+    got = to_np(DeviceStep(b).run())
+    assert_tolerance(got, oracle_packed(b))

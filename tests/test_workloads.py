@@ -69,3 +69,41 @@ def test_padding_count_matches_the_blog_example():
     # the real tokens keep their positions: each sequence's last rows are its real ones
     assert np.array_equal(pb.context_lens - pb.q_len, b.p)
     assert np.array_equal(pb.context_lens[:-1], b.p[:-1] + 100)
+
+
+def test_compiled_generator_equals_numpy_bitwise():
+    """The compiled host generator (used for the oracle's large inputs) gives
+    the numpy definition's bits, over seeds above 2^32, every kind, layers,
+    large sequence ids and positions, scattered heads, both dtypes."""
+    assert w._values_lib() is not None, "gcc should build hostgen/token_values.c"
+    rng = np.random.default_rng(17)
+    for seed, kind, layer, seq, dtype in [(0, 0, 0, 0, "bf16"), (2 ** 40 + 12345, 1, 31, 1999, "bf16"),
+                                          (0xFFFF_FFFF_FFFF, 2, 65535, 2 ** 31 + 7, "f32"),
+                                          (7, 1, 3, 123456, "f32")]:
+        pos = np.concatenate([np.arange(40), rng.integers(0, 2 ** 32 - 1, 24)])
+        heads = [0, 5, 31, 1000]
+        a = w.token_values_numpy(seed, kind, layer, seq, pos, heads, 128, dtype)
+        b = w.token_values(seed, kind, layer, seq, pos, heads, 128, dtype)
+        assert a.shape == b.shape == (64, 4, 128)
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    # head_dim 64 and an empty request
+    a = w.token_values_numpy(3, 2, 1, 9, np.arange(5), range(4), 64, "f32")
+    assert np.array_equal(a.view(np.uint32), w.token_values(3, 2, 1, 9, np.arange(5), range(4), 64, "f32").view(np.uint32))
+    assert w.token_values(3, 2, 1, 9, np.arange(0), range(4), 64, "f32").shape == (0, 4, 64)
+
+
+def test_drift_shapes_scores_only_through_q_and_k():
+    """A drifted batch adds q_shift * u to every query and k_slope * j * u to
+    the key at position j (u = ones / sqrt(A)), rounded to the dtype; values
+    are untouched and the undrifted batch is the plain generator."""
+    plain = w.make_batch([10], [3], num_heads=2, head_dim=128, block_size=16, dtype="f32", seed=4)
+    drift = w.make_batch([10], [3], num_heads=2, head_dim=128, block_size=16, dtype="f32", seed=4,
+                         drift=(4.0, 0.5))
+    u = 1 / np.sqrt(128)
+    np.testing.assert_allclose(drift.history(0, w.KIND_K) - plain.history(0, w.KIND_K),
+                               (0.5 * np.arange(13) * u)[:, None, None] * np.ones((1, 2, 128)), atol=1e-5)
+    np.testing.assert_allclose(drift.packed(w.KIND_Q) - plain.packed(w.KIND_Q), 4.0 * u, atol=1e-6)
+    assert np.array_equal(drift.history(0, w.KIND_V), plain.history(0, w.KIND_V))
+    bf = w.make_batch([10], [3], num_heads=2, head_dim=128, block_size=16, dtype="bf16", seed=4, drift=(4.0, 0.5))
+    k = bf.history(0, w.KIND_K)
+    assert np.array_equal(k, w.round_to_bf16(k))
