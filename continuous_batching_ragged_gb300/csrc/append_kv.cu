@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kThreads) append_kv_kernel(
 
 cb_status append(const void* k_new, const void* v_new, const int64_t* slot_mapping, int32_t num_tokens,
                  const int32_t* dims, const cb_kv_cache* cache, void* stream, const char* who) {
+  cb::NvtxRange nvtx("cb.append_kv");
   if (!cache) return cb::fail(CB_ERR_INVALID, "%s: null cache", who);
   if (num_tokens < 0) return cb::fail(CB_ERR_INVALID, "%s: num_tokens < 0", who);
   if (cache->num_blocks < 1 || cache->block_size < 1 || cache->num_heads < 1 || cache->head_dim < 1)

@@ -486,6 +486,7 @@ cb_status step_plan_layout(void* workspace, size_t workspace_bytes, int32_t num_
 }
 
 cb_status launch_plan(const AttnArgs& a, const StepPlan& plan, cudaStream_t stream) {
+  NvtxRange nvtx("cb.plan");
   plan_step_kernel<<<1, kPlanThreads, 0, stream>>>(a, plan);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "step plan: launch");

@@ -835,6 +835,7 @@ bool g_attr_set[64] = {};
 }  // namespace
 
 cb_status launch_prefill_tc(const AttnArgs& a, const StepPlan& plan, bool after_plan, cudaStream_t stream) {
+  NvtxRange nvtx("cb.prefill");
   if (a.dtype != CB_DTYPE_BF16 || a.head_dim != HD)
     return fail(CB_ERR_UNSUPPORTED, "prefill chunks: bf16 with head_dim 128 only");
   const int B = a.block_size;

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <utility>
 
@@ -36,6 +37,17 @@ void unlock_aux();
 
 // Number of SMs of the current device.
 int sm_count();
+
+// A named NVTX range over a host scope (header-only NVTX v3: without an
+// attached profiler each push/pop is a cheap no-op).  Marks the launches of
+// the append, the step plan, the decode and the prefill kernels, so a
+// timeline shows which host call enqueued which kernels.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 cb_status cuda_fail(cudaError_t err, const char* what);
 

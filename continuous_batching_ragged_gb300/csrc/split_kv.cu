@@ -809,6 +809,7 @@ static bool persistent_ok(const AttnArgs& a) {
 
 cb_status launch_decode_persistent(const AttnArgs& a, const StepPlan& plan, bool after_plan,
                                    bool wait_previous, cudaStream_t stream) {
+  NvtxRange nvtx("cb.decode");
   SplitArgs sa;
   sa.wait_previous = wait_previous ? 1 : 0;
   sa.a = a;
@@ -866,6 +867,7 @@ cb_status launch_decode_persistent(const AttnArgs& a, const StepPlan& plan, bool
 
 cb_status launch_split_kv(const AttnArgs& a, bool row_mode, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream) {
+  NvtxRange nvtx("cb.decode_rows");
   const int32_t rows = row_mode ? a.num_tokens : a.num_seqs;
   if (rows == 0) return CB_OK;
   if (!row_mode) {
