@@ -57,12 +57,12 @@ def make_workload(name: str, decode_seqs: int = 256):
         return (W.mixed_step(num_kv_heads=8),
                 "mixed_gqa_m2048_64decode_ctx256-4096_chunks661-661-662_bf16_Hq32_Hkv8_A128_B16")
     if name == "mixed_padded":
-        return W.padded_equivalent(W.mixed_step()), "mixed_m2048_left_padded_to_67x662_bf16_H32_A128_B16"
+        return W.left_padded(W.mixed_step()), "mixed_m2048_left_padded_to_67x662_masked_bf16_H32_A128_B16"
     if name == "insertion":
         return W.page_insertion_example(), "insertion_B8_n100_ragged_bf16_H32_A128_B16"
     if name == "insertion_padded":
-        return (W.padded_equivalent(W.page_insertion_example()),
-                "insertion_B8_n100_left_padded_8x100_bf16_H32_A128_B16")
+        return (W.left_padded(W.page_insertion_example()),
+                "insertion_B8_n100_left_padded_8x100_masked_bf16_H32_A128_B16")
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -188,7 +188,8 @@ class Staged:
                 api.cb_synth_fill_cache(pool, b.seed, kind, b.layer, sid, pl, bt, int(b.p.max()))
         rows = torch.from_numpy(np.repeat(b.seq_ids, b.q_len)).cuda()
         pos = torch.from_numpy(np.concatenate(
-            [np.arange(b.p[s], b.p[s] + b.q_len[s]) for s in range(b.num_seqs)]).astype(np.int32)).cuda()
+            [b.gen_positions(s, np.arange(b.p[s], b.p[s] + b.q_len[s])) for s in range(b.num_seqs)])
+            .astype(np.int32)).cuda()
         self.q, self.k_new, self.v_new = (torch.empty((b.T, b.heads_of(kind), b.head_dim), dtype=dt, device="cuda")
                                           for kind in (W.KIND_Q, W.KIND_K, W.KIND_V))
         for kind, t in ((W.KIND_Q, self.q), (W.KIND_K, self.k_new), (W.KIND_V, self.v_new)):
@@ -204,6 +205,7 @@ class Staged:
         self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device="cuda")
         self.scale = 1.0 / math.sqrt(b.head_dim)
         self.api = api
+        self.pads = None if b.pad_lens is None else torch.from_numpy(b.pad_lens.astype(np.int32)).cuda()
 
     def append(self, stream=None, k=None, v=None, slots=None):
         self.api.cb_append_kv(self.k_new if k is None else k, self.v_new if v is None else v,
@@ -211,10 +213,16 @@ class Staged:
 
     def attend(self, stream=None, q=None, cu=None, ctx=None, bt=None, out=None):
         b = self.b
-        fn = self.api.cb_ragged_attention_gqa if self.grouped else self.api.cb_ragged_attention
-        fn(self.q if q is None else q, self.cache, self.cu if cu is None else cu, self.ctx if ctx is None else ctx,
-           self.bt if bt is None else bt, max_q_len=b.max_q_len, max_context_len=b.max_context_len,
-           scale=self.scale, out=self.out if out is None else out, workspace=self.ws, stream=stream)
+        args = (self.q if q is None else q, self.cache, self.cu if cu is None else cu,
+                self.ctx if ctx is None else ctx, self.bt if bt is None else bt)
+        kw = dict(max_q_len=b.max_q_len, max_context_len=b.max_context_len, scale=self.scale,
+                  out=self.out if out is None else out, workspace=self.ws, stream=stream)
+        if self.pads is not None:
+            self.api.cb_padded_attention(*args, self.pads, **kw)
+        elif self.grouped:
+            self.api.cb_ragged_attention_gqa(*args, **kw)
+        else:
+            self.api.cb_ragged_attention(*args, **kw)
 
 
 # ---------------------------------------------------------------------------

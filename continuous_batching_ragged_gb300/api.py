@@ -110,6 +110,26 @@ def cb_ragged_attention(q: torch.Tensor, cache: KVCache, cu_seqlens_q: torch.Ten
     return out
 
 
+def cb_padded_attention(q: torch.Tensor, cache: KVCache, cu_seqlens_q: torch.Tensor,
+                        context_lens: torch.Tensor, block_tables: torch.Tensor, pad_lens: torch.Tensor, *,
+                        max_q_len: int, max_context_len: int, scale: float, out: torch.Tensor,
+                        workspace: Optional[torch.Tensor], stream=None) -> torch.Tensor:
+    """cb_padded_attention: a left-padded batch; the first pad_lens[s] rows of
+    sequence s are padding (masked keys, rows not written)."""
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("context_lens", context_lens),
+                    ("block_tables", block_tables), ("pad_lens", pad_lens)):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    c = cache.c_struct()
+    ws_ptr = _ptr(workspace) if workspace is not None and workspace.numel() else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(native.lib().cb_padded_attention(
+        _ptr(q), ctypes.byref(c), _ptr(cu_seqlens_q), _ptr(context_lens), _ptr(block_tables), _ptr(pad_lens),
+        context_lens.shape[0], q.shape[0], block_tables.shape[1], max_q_len, max_context_len,
+        float(scale), _ptr(out), ws_ptr, ws_bytes, _stream_handle(stream)), "cb_padded_attention")
+    return out
+
+
 def cb_attention_workspace_size_gqa(cache: KVCache, num_q_heads: int, num_seqs: int, num_tokens: int,
                                     max_context_len: int) -> int:
     c = cache.c_struct()

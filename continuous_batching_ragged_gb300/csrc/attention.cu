@@ -146,13 +146,17 @@ cb_status attention(const char* who, const void* q, int32_t num_q_heads, const c
                     const int32_t* cu_seqlens_q, const int32_t* context_lens, const int32_t* block_tables,
                     int32_t num_seqs, int32_t num_tokens, int32_t max_blocks_per_seq, int32_t max_q_len,
                     int32_t max_context_len, float scale, void* out, void* workspace, size_t workspace_bytes,
-                    void* stream) {
+                    void* stream, const int32_t* pad_lens = nullptr) {
   cb::AttnArgs a;
   cb_status st = prepare(who, q, cache, cu_seqlens_q, context_lens, block_tables, num_seqs, num_tokens,
                          max_blocks_per_seq, max_q_len, max_context_len, scale, out, nullptr, false, a, num_q_heads);
   if (st != CB_OK || num_seqs == 0) return st;
+  a.pad_lens = pad_lens;
   cudaStream_t main = static_cast<cudaStream_t>(stream);
-  if (cache->dtype == CB_DTYPE_F32) return cb::launch_split_kv(a, true, workspace, workspace_bytes, main);
+  if (cache->dtype == CB_DTYPE_F32) {
+    if (pad_lens) return cb::fail(CB_ERR_UNSUPPORTED, "%s: padded batches need a bf16 cache", who);
+    return cb::launch_split_kv(a, true, workspace, workspace_bytes, main);
+  }
 
   // bf16: the step plan first, then the persistent kernels over its work lists
   cb::StepPlan plan;
@@ -183,6 +187,19 @@ extern "C" cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache
   return attention("cb_ragged_attention", q, 0, cache, cu_seqlens_q, context_lens, block_tables, num_seqs,
                    num_tokens, max_blocks_per_seq, max_q_len, max_context_len, scale, out, workspace,
                    workspace_bytes, stream);
+}
+
+extern "C" cb_status cb_padded_attention(const void* q, const cb_kv_cache* cache,
+                                         const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                         const int32_t* block_tables, const int32_t* pad_lens,
+                                         int32_t num_seqs, int32_t num_tokens, int32_t max_blocks_per_seq,
+                                         int32_t max_q_len, int32_t max_context_len, float scale,
+                                         void* out, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+  if (!pad_lens && num_seqs > 0) return cb::fail(CB_ERR_INVALID, "cb_padded_attention: null pad_lens");
+  return attention("cb_padded_attention", q, 0, cache, cu_seqlens_q, context_lens, block_tables, num_seqs,
+                   num_tokens, max_blocks_per_seq, max_q_len, max_context_len, scale, out, workspace,
+                   workspace_bytes, stream, pad_lens);
 }
 
 extern "C" size_t cb_attention_workspace_size_gqa(const cb_kv_cache* cache, int32_t num_q_heads,

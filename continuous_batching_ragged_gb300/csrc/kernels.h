@@ -34,6 +34,11 @@ struct AttnArgs {
   // null.  When set, the four host sizes above are capacities: buffer extents
   // that bound the device values, which only the step plan reads.
   const int32_t* dims = nullptr;
+  // Left padding (cb_padded_attention), or null: the first pad_lens[s] rows
+  // of sequence s's chunk are padding, their keys (positions p_s ..
+  // p_s + pad - 1) are masked out of every row and their rows are not
+  // written.  0 <= pad < q_len (the plan leaves a row out otherwise).
+  const int32_t* pad_lens = nullptr;
 };
 
 // Keys per split of the register split-KV kernel, and the smallest split of

@@ -133,6 +133,10 @@ __device__ __forceinline__ RowInfo row_info(const AttnArgs& a, const StepSizes& 
   r.ctx = a.context_lens[s];
   r.bad = r.q_len < 1 || r.ctx < r.q_len || r.ctx > z.max_context_len || r.q_len > z.max_q_len || c0 < 0 ||
           c1 > z.num_tokens || (int64_t(r.ctx) + a.block_size - 1) / a.block_size > a.max_blocks_per_seq;
+  if (a.pad_lens && !r.bad) {
+    const int pad = a.pad_lens[s];
+    r.bad = pad < 0 || pad >= r.q_len;           // a chunk keeps at least one real row
+  }
   return r;
 }
 

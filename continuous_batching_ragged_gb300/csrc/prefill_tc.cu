@@ -285,7 +285,7 @@ __device__ __forceinline__ void load_kv_tile_ring(uint32_t dst, const CUtensorMa
 // segments, whose results then go to partial slots slot0 + j0 / segment).
 struct WorkItem {
   int u;                                           // entry index; >= the entry count: no more work
-  int s, h, row0, c0, q_len, ctx, j0, j1, slot0, pad0, pad1;
+  int s, h, row0, c0, q_len, ctx, j0, j1, slot0, pad, spare;   // pad: left-padding rows of the chunk
 };
 static_assert(sizeof(WorkItem) == 48, "work item slot");
 
@@ -327,6 +327,10 @@ struct PrefillWork {
 // items that the V loader, the MMA thread and the softmax warps read in the
 // same order; every barrier phase runs on across units, so the next unit's K
 // tiles and Q load overlap the end of the current one.
+// PADDED: the instantiation for left-padded batches (cb_padded_attention),
+// which masks each chunk's pad keys and skips its pad rows' stores; the
+// ragged path's instantiation carries none of that code.
+template <bool PADDED>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const AttnArgs a, const PrefillWork w) {
@@ -436,8 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             it.c0 = __ldcg(a.cu_seqlens_q + it.s);
             it.q_len = __ldcg(a.cu_seqlens_q + it.s + 1) - it.c0;
             it.ctx = __ldcg(a.context_lens + it.s);
+            it.pad = PADDED ? __ldcg(a.pad_lens + it.s) : 0;
             bad = it.c0 < 0 || it.q_len < 2 || it.c0 + it.q_len > a.num_tokens || it.row0 >= it.q_len ||
-                  it.ctx < it.q_len || it.ctx > a.max_context_len;
+                  it.ctx < it.q_len || it.ctx > a.max_context_len || it.pad < 0 || it.pad >= it.q_len;
             if (!bad) {
               const UnitShape sh = unit_shape(it);
               bad = it.j1 > sh.n_tiles ||
@@ -705,6 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qi = it.row0 + BM * t + i;         // row within the chunk
       const int limit = min(sh.p + qi, it.ctx - 1);  // last key this row sees
       const int warp_limit = min(sh.p + it.row0 + BM * t + 32 * wq, it.ctx - 1);   // smallest in the warp
+      // left padding: keys sh.p .. sh.p + pad - 1 are masked for every row
+      const int pad_k0 = sh.p, pad_n = PADDED ? it.pad : 0;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; ok && j < sh.n; ++j) {
         if (!mbar_wait(bar(BAR_S + t), (cnt + j) & 1)) {
@@ -722,6 +729,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < BN; ++c)
             if (kb + c > limit) sr[c] = __float_as_uint(-INFINITY);
+        }
+        if (PADDED && kb < pad_k0 + pad_n && kb + BN > pad_k0) {   // the tile holds pad keys: mask them
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (unsigned(kb + c - pad_k0) < unsigned(pad_n)) sr[c] = __float_as_uint(-INFINITY);
         }
         {                                          // four independent max chains (latency, not issue, bound)
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -789,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int e_row = it.c0 + qi, e_h = it.h, e_slot0 = it.slot0, e_j0 = sh.j0, e_ntiles = sh.n_tiles;
-      const bool e_real = qi < it.q_len;
+      const bool e_real = qi < it.q_len && (!PADDED || qi >= it.pad);   // padding rows are not written
       __nv_bfloat16* const e_dst = static_cast<__nv_bfloat16*>(a.out) + (size_t(e_row) * H + e_h) * HD;
       if (e_slot0 < 0) {
         const float inv = 1.0f / l;
@@ -830,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 std::mutex g_attr_mutex;
-bool g_attr_set[64] = {};
+bool g_attr_set[2][64] = {};
 
 }  // namespace
 
@@ -873,11 +885,12 @@ cb_status launch_prefill_tc(const AttnArgs& a, const StepPlan& plan, bool after_
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64) {
     std::lock_guard<std::mutex> lock(g_attr_mutex);   // first calls may race from several host threads
-    if (!g_attr_set[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           int(kSmemBytes));
+    const int v = a.pad_lens ? 1 : 0;
+    if (!g_attr_set[v][dev]) {
+      cudaError_t e = cudaFuncSetAttribute(v ? prefill_tc_kernel<true> : prefill_tc_kernel<false>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
       if (e != cudaSuccess) return cuda_fail(e, "prefill chunks: shared memory attribute");
-      g_attr_set[dev] = true;
+      g_attr_set[v][dev] = true;
     }
   }
   PrefillWork w;
@@ -892,8 +905,9 @@ cb_status launch_prefill_tc(const AttnArgs& a, const StepPlan& plan, bool after_
   const int64_t max_units = int64_t(plan.pre_cap) * a.num_heads + kPrefillSegSlots;
   const int64_t grid = std::min<int64_t>(sm_count(), max_units);
   if (grid < 1) return CB_OK;
-  cudaError_t e = launch_kernel(prefill_tc_kernel, dim3(unsigned(grid)), dim3(kThreads), kSmemBytes, stream,
-                                after_plan, tq, tk, tv, a, w);
+  cudaError_t e = launch_kernel(a.pad_lens ? prefill_tc_kernel<true> : prefill_tc_kernel<false>,
+                                dim3(unsigned(grid)), dim3(kThreads), kSmemBytes, stream, after_plan, tq, tk, tv,
+                                a, w);
   if (e != cudaSuccess) return cuda_fail(e, "prefill chunks: launch");
   return CB_OK;
 }

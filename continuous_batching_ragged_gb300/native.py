@@ -22,7 +22,7 @@ EXPORTS = ("cb_append_kv", "cb_attention_workspace_size", "cb_ragged_attention",
            "cb_append_kv_dims", "cb_plan_step", "cb_ragged_attention_planned",
            "cb_ragged_attention_gqa", "cb_attention_workspace_size_gqa",
            "cb_plan_step_gqa", "cb_ragged_attention_planned_gqa",
-           "cb_decode_attention_noalloc",
+           "cb_decode_attention_noalloc", "cb_padded_attention",
            "cb_scheduler_create", "cb_scheduler_destroy", "cb_add_request", "cb_build_batch",
            "cb_complete_step", "cb_scheduler_stats", "cb_check_device_errors", "cb_last_error",
            "cb_synth_tokens", "cb_synth_fill_cache", "cb_selftest_bounded_wait")
@@ -89,6 +89,7 @@ def lib() -> ctypes.CDLL:
         "cb_ragged_attention_gqa": (st, [vp, i32, pcache, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, sz,
                                          vp]),
         "cb_attention_workspace_size_gqa": (sz, [pcache, i32, i32, i32, i32]),
+        "cb_padded_attention": (st, [vp, pcache, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, sz, vp]),
         "cb_plan_step": (st, [pcache, vp, vp, vp, i32, i32, i32, i32, i32, vp, sz, vp]),
         "cb_ragged_attention_planned": (st, [vp, pcache, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp,
                                              sz, vp]),

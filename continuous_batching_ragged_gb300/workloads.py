@@ -220,6 +220,12 @@ class RaggedBatch:
     # such a batch exist only on the host (the device generator does not
     # shape them).
     drift: Optional[Tuple[float, float]] = None
+    # Left padding (a padded batch, see left_padded): the first pad_lens[s]
+    # new tokens of sequence s are pad tokens.  They occupy cache positions
+    # p .. p + pad - 1 and take their values from generator positions
+    # PAD_POSITION_BASE + i; the real tokens after them keep the values of
+    # their unpadded positions, so real rows see exactly the unpadded data.
+    pad_lens: Optional[np.ndarray] = None
 
     @property
     def kv_heads(self) -> int:
@@ -273,9 +279,19 @@ class RaggedBatch:
         return 2 if self.dtype == "bf16" else 4
 
     # -- values ------------------------------------------------------------
+    def gen_positions(self, s: int, positions) -> np.ndarray:
+        """Generator positions of sequence s's cache positions (the identity
+        unless the batch is left-padded)."""
+        x = np.asarray(positions, dtype=np.int64)
+        if self.pad_lens is None or int(self.pad_lens[s]) == 0:
+            return x
+        p, pad = int(self.p[s]), int(self.pad_lens[s])
+        return np.where(x < p, x, np.where(x < p + pad, PAD_POSITION_BASE + (x - p), x - pad))
+
     def values(self, kind: int, s: int, positions, heads) -> np.ndarray:
-        """Values of ``kind`` for sequence s at ``positions`` and ``heads``:
+        """Values of ``kind`` for sequence s at cache ``positions`` and ``heads``:
         [len(positions), len(heads), A], fp32 holding dtype values."""
+        positions = self.gen_positions(s, positions)
         x = token_values(self.seed, kind, self.layer, int(self.seq_ids[s]), positions, heads,
                          self.head_dim, self.dtype)
         if self.drift is None or kind == KIND_V:
@@ -365,19 +381,34 @@ def make_batch(p: Sequence[int], q_len: Sequence[int], *, num_heads: int, head_d
                        drift=drift)
 
 
-def padded_equivalent(b: RaggedBatch) -> RaggedBatch:
-    """The same sequences as one rectangular, left-padded batch: every sequence
-    carries max(q_len) new tokens, its real ones last, so a step computes
-    B * max(q_len) query rows and the pad tokens' keys.  (Hugging Face blog
-    "Continuous batching from first principles", section "Continuous
-    batching": inserting an n-token prompt into B decoding prompts costs
-    (n-1)(B-1) padding tokens.)"""
+PAD_POSITION_BASE = 1 << 30      # generator positions of pad tokens (no real token sits there)
+
+
+def left_padded(b: RaggedBatch) -> RaggedBatch:
+    """The same sequences as one rectangular, left-padded batch (Hugging Face
+    blog "Continuous batching from first principles", section "Continuous
+    batching": without ragged batching, sequences are padded on the left to a
+    common length and masked; inserting an n-token prompt into B decoding
+    prompts costs (n-1)(B-1) padding tokens).  Every sequence carries
+    n = max(q_len) new tokens, pad_lens = n - q_len of them pads first; the
+    pads are appended to the cache like real tokens and masked out of
+    attention by cb_padded_attention, so a step computes B * n query rows
+    over the pads' keys too, while each real row's result is that of the
+    ragged batch."""
     n = int(b.q_len.max())
     pb = make_batch(b.p, np.full(b.num_seqs, n, np.int64), num_heads=b.num_heads, head_dim=b.head_dim,
                     block_size=b.block_size, dtype=b.dtype, seed=b.seed, layer=b.layer,
-                    seq_ids=b.seq_ids, name=b.name + "_padded")
+                    seq_ids=b.seq_ids, name=b.name + "_padded", num_kv_heads=b.num_kv_heads)
+    pb.pad_lens = (n - b.q_len).astype(np.int32)
     pb.useful_tokens = b.T
     return pb
+
+
+def real_rows(pb: RaggedBatch) -> np.ndarray:
+    """Packed row indices of a left-padded batch's real (non-pad) rows, in
+    packed order of the unpadded batch."""
+    cu = pb.cu_seqlens_q
+    return np.concatenate([np.arange(cu[s] + int(pb.pad_lens[s]), cu[s + 1]) for s in range(pb.num_seqs)])
 
 
 def padding_tokens(b: RaggedBatch) -> int:

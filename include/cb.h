@@ -224,6 +224,35 @@ cb_status cb_ragged_attention_planned_gqa(const void* q, int32_t num_q_heads, co
                                           void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * cb_padded_attention -- attention of a left-padded rectangular batch, the
+ * padded batching that ragged batching replaces.
+ * Hugging Face blog "Continuous batching from first principles", section
+ * "Continuous batching": without ragged batching, the sequences of a batch
+ * are padded on the left to one common length and an attention mask keeps
+ * the pad positions out of the softmax; inserting an n-token prompt into a
+ * batch of B decoding sequences costs (n - 1)(B - 1) pad tokens.
+ *
+ * Same arguments and layout as cb_ragged_attention, plus
+ *   pad_lens  device int32 [num_seqs]: the first pad_lens[s] rows of
+ *             sequence s's chunk are padding (their K/V were appended like
+ *             any other token).  With p_s = context_lens[s] - q_len_s, real
+ *             row i (pad_lens[s] <= i < q_len_s) attends keys 0 .. p_s - 1 and
+ *             p_s + pad_lens[s] .. p_s + i: the pad keys are masked out of
+ *             every row.  The pad rows' own output rows are not written.
+ * Needs a bf16 cache (CB_ERR_UNSUPPORTED otherwise) and
+ * 0 <= pad_lens[s] < q_len_s; a sequence breaking that is left out and
+ * reported as CB_ERR_INVALID by cb_check_device_errors.  Rows are computed at
+ * the padded batch's full cost: every pad row and pad key goes through the
+ * same kernels as real ones.
+ * ------------------------------------------------------------------------- */
+cb_status cb_padded_attention(const void* q, const cb_kv_cache* cache, const int32_t* cu_seqlens_q,
+                              const int32_t* context_lens, const int32_t* block_tables,
+                              const int32_t* pad_lens, int32_t num_seqs, int32_t num_tokens,
+                              int32_t max_blocks_per_seq, int32_t max_q_len, int32_t max_context_len,
+                              float scale, void* out, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* ---------------------------------------------------------------------------
  * cb_decode_attention_noalloc -- decode attention that allocates nothing.
  * The sources have no counterpart: this is a deployment variant of the decode
  * rows of cb_ragged_attention for callers that cannot allocate device memory

@@ -86,6 +86,42 @@ def attend_sequence(q: np.ndarray, k: np.ndarray, v: np.ndarray, p: int, scale: 
     return out
 
 
+def attend_left_padded(q: np.ndarray, k: np.ndarray, v: np.ndarray, p: int, pad: int,
+                       scale: float) -> np.ndarray:
+    """Attention of one left-padded chunk, the padded batching that ragged
+    batching replaces (Hugging Face blog "Continuous batching from first
+    principles", section "Continuous batching": sequences padded on the left
+    to a common length, an attention mask keeping the pads out).
+
+    q: [n, H, A] the chunk's rows, its `pad` pad rows first; k, v: [p + n,
+    H_kv, A] the history, with the pad tokens' keys and values at positions
+    p .. p + pad - 1.  Real row i (pad <= i < n) attends the keys j <= p + i
+    that are not pads: j < p or j >= p + pad.  Pad rows have no output and
+    come back as NaN.  Returns [n, H, A] fp64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n, H, A = q.shape
+    c, H_kv = k.shape[0], k.shape[1]
+    if c != p + n or v.shape[0] != c:
+        raise ValueError("history length must equal p + q_len")
+    if not 0 <= pad < n:
+        raise ValueError("need 0 <= pad < q_len")
+    group = H // H_kv
+    out = np.full((n, H, A), np.nan)
+    j = np.arange(c)
+    rows = np.arange(pad, n)
+    visible = (j[None, :] <= (p + rows)[:, None]) & ((j[None, :] < p) | (j[None, :] >= p + pad))
+    for h in range(H):
+        z = scale * (q[pad:, h, :] @ k[:, h // group, :].T)
+        z = np.where(visible, z, -np.inf)
+        m = z.max(axis=1, keepdims=True)
+        w = np.exp(z - m)
+        out[pad:, h, :] = (w @ v[:, h // group, :]) / w.sum(axis=1, keepdims=True)
+    return out
+
+
 def ragged_attention(q_packed: np.ndarray, cu_seqlens_q: np.ndarray, context_lens: np.ndarray,
                      k_hist, v_hist, scale: float) -> np.ndarray:
     """Attention over a packed batch, each sequence computed alone and unpacked.

@@ -87,7 +87,8 @@ class DeviceStep:
             self.v_new = dev(b.packed(W.KIND_V), b.dtype)
         else:
             seq_rows = np.repeat(b.seq_ids, b.q_len)
-            pos = np.concatenate([np.arange(b.p[s], b.p[s] + b.q_len[s]) for s in range(b.num_seqs)])
+            pos = np.concatenate([b.gen_positions(s, np.arange(b.p[s], b.p[s] + b.q_len[s]))
+                                  for s in range(b.num_seqs)])
             sid = torch.from_numpy(seq_rows.astype(np.int64)).cuda()
             ps = torch.from_numpy(pos.astype(np.int32)).cuda()
             self.q, self.k_new, self.v_new = (torch.empty((T, b.heads_of(kind), b.head_dim), dtype=dt, device="cuda")
@@ -101,6 +102,7 @@ class DeviceStep:
         self.out = torch.empty_like(self.q)
         fill_sentinel(self.out)
         self.grouped = b.num_heads != b.kv_heads
+        self.pads = None if b.pad_lens is None else torch.from_numpy(b.pad_lens.astype(np.int32)).cuda()
         ws = (api.cb_attention_workspace_size_gqa(self.cache, b.num_heads, b.num_seqs, T, b.max_context_len)
               if self.grouped else api.cb_attention_workspace_size(self.cache, b.num_seqs, T, b.max_context_len))
         self.ws = torch.empty(ws, dtype=torch.uint8, device="cuda")
@@ -126,9 +128,13 @@ class DeviceStep:
 
     def attend(self):
         b = self.b
-        fn = api.cb_ragged_attention_gqa if self.grouped else api.cb_ragged_attention
-        fn(self.q, self.cache, self.cu, self.ctx, self.bt, max_q_len=b.max_q_len,
-           max_context_len=b.max_context_len, scale=self.scale, out=self.out, workspace=self.ws)
+        kw = dict(max_q_len=b.max_q_len, max_context_len=b.max_context_len, scale=self.scale, out=self.out,
+                  workspace=self.ws)
+        if self.pads is not None:
+            api.cb_padded_attention(self.q, self.cache, self.cu, self.ctx, self.bt, self.pads, **kw)
+        else:
+            fn = api.cb_ragged_attention_gqa if self.grouped else api.cb_ragged_attention
+            fn(self.q, self.cache, self.cu, self.ctx, self.bt, **kw)
 
     def run(self):
         self.append()

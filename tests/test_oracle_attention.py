@@ -277,3 +277,61 @@ def test_grouped_query_attention_rejects_uneven_groups():
     k = np.zeros((1, 4, 4))
     with pytest.raises(ValueError):
         oa.attend_sequence(q, k, k, 0, 1.0)
+
+
+def test_left_padded_real_rows_equal_unpadded_attention():
+    """A left-padded chunk's real rows see exactly the unpadded chunk's keys:
+    inserting pad tokens (masked) between the cache and the real tokens
+    changes no real row.  Pad rows have no output."""
+    from oracle import attention as oa
+    rng = np.random.default_rng(8)
+    p, n, pad, H, Hkv, A = 5, 7, 3, 4, 2, 16
+    q = rng.standard_normal((n - pad, H, A))
+    k = rng.standard_normal((p + n - pad, Hkv, A))
+    v = rng.standard_normal((p + n - pad, Hkv, A))
+    ref = oa.attend_sequence(q, k, v, p, 0.3)
+    # the padded layout: pad rows (arbitrary values) first, pad keys at p .. p+pad-1
+    qp = np.concatenate([rng.standard_normal((pad, H, A)) * 50, q])
+    kp = np.concatenate([k[:p], rng.standard_normal((pad, Hkv, A)) * 50, k[p:]])
+    vp = np.concatenate([v[:p], rng.standard_normal((pad, Hkv, A)) * 50, v[p:]])
+    got = oa.attend_left_padded(qp, kp, vp, p, pad, 0.3)
+    assert np.all(np.isnan(got[:pad]))
+    np.testing.assert_allclose(got[pad:], ref, rtol=0, atol=1e-12)
+    # no padding: the plain definition
+    np.testing.assert_allclose(oa.attend_left_padded(q, k, v, p, 0, 0.3), ref, rtol=0, atol=1e-12)
+
+
+def test_left_padded_hand_example():
+    """p = 2 cached keys, a 3-row chunk with 2 pad rows: its one real row
+    (chunk row 2, position 4) attends keys 0, 1 and 4 only."""
+    from oracle import attention as oa
+    q = np.zeros((3, 1, 2))
+    q[2, 0] = [1.0, 0.0]
+    k = np.array([[1.0, 0.0], [2.0, 0.0], [9.0, 0.0], [9.0, 0.0], [0.0, 0.0]])[:, None, :]
+    v = np.array([[1.0, 0.0], [0.0, 1.0], [100.0, 100.0], [100.0, 100.0], [3.0, 3.0]])[:, None, :]
+    got = oa.attend_left_padded(q, k, v, 2, 2, 1.0)[2, 0]
+    w = np.exp(np.array([1.0, 2.0, 0.0]))
+    w /= w.sum()
+    exp = w[0] * v[0, 0] + w[1] * v[1, 0] + w[2] * v[4, 0]
+    np.testing.assert_allclose(got, exp, rtol=0, atol=1e-14)
+
+
+def test_left_padded_batch_layout():
+    """workloads.left_padded: every sequence gets max(q_len) rows with the pads
+    first; real rows carry the unpadded batch's q/k/v values and the history
+    of a real row is the unpadded history with the pad tokens inserted at
+    p .. p + pad - 1; the blog's insertion example costs (n-1)(B-1) pads."""
+    from continuous_batching_ragged_gb300 import workloads as W
+    b = W.make_batch([4, 0, 9], [1, 6, 2], num_heads=2, head_dim=8, block_size=4, dtype="bf16", seed=12)
+    pb = W.left_padded(b)
+    assert pb.q_len.tolist() == [6, 6, 6] and pb.pad_lens.tolist() == [5, 0, 4] and pb.useful_tokens == 9
+    rr = W.real_rows(pb)
+    for kind in (W.KIND_Q, W.KIND_K, W.KIND_V):
+        assert np.array_equal(pb.packed(kind)[rr], b.packed(kind))
+    for s in range(3):
+        p, pad = int(b.p[s]), int(pb.pad_lens[s])
+        h = pb.history(s, W.KIND_K)
+        ref = b.history(s, W.KIND_K)
+        assert np.array_equal(np.concatenate([h[:p], h[p + pad:]]), ref)
+    ins = W.page_insertion_example(num_heads=2, head_dim=8)
+    assert W.padding_tokens(ins) == 99 * 7 == int(W.left_padded(ins).pad_lens.sum())

@@ -64,11 +64,12 @@ def test_padding_count_matches_the_blog_example():
     b = w.page_insertion_example()
     assert b.T == 7 + 100
     assert w.padding_tokens(b) == 693 == (100 - 1) * (8 - 1)
-    pb = w.padded_equivalent(b)
-    assert pb.T == 8 * 100 and pb.T - b.T == 693
-    # the real tokens keep their positions: each sequence's last rows are its real ones
+    pb = w.left_padded(b)
+    assert pb.T == 8 * 100 and pb.T - b.T == 693 == int(pb.pad_lens.sum())
+    # pads come first in each chunk, after the cached prefix; the real rows follow
     assert np.array_equal(pb.context_lens - pb.q_len, b.p)
     assert np.array_equal(pb.context_lens[:-1], b.p[:-1] + 100)
+    assert pb.pad_lens.tolist() == [99] * 7 + [0]
 
 
 def test_compiled_generator_equals_numpy_bitwise():
