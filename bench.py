@@ -53,6 +53,12 @@ def make_workload(name: str, decode_seqs: int = 256):
     if name == "decode_gqa":
         return (W.decode_step(num_seqs=decode_seqs, num_kv_heads=8),
                 f"decode_gqa_{decode_seqs}seq_ctx512-4096_bf16_Hq32_Hkv8_A128_B16")
+    if name == "decode_gqa_kv4":
+        return (W.decode_step(num_seqs=decode_seqs, num_kv_heads=4),
+                f"decode_gqa_{decode_seqs}seq_ctx512-4096_bf16_Hq32_Hkv4_A128_B16")
+    if name == "decode_mqa":
+        return (W.decode_step(num_seqs=decode_seqs, num_kv_heads=1),
+                f"decode_mqa_{decode_seqs}seq_ctx512-4096_bf16_Hq32_Hkv1_A128_B16")
     if name == "mixed_gqa":
         return (W.mixed_step(num_kv_heads=8),
                 "mixed_gqa_m2048_64decode_ctx256-4096_chunks661-661-662_bf16_Hq32_Hkv8_A128_B16")
@@ -907,7 +913,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=["decode", "mixed", "long", "tiny", "trace", "trace_graph",
-                                                             "decode_gqa", "mixed_gqa", "mixed_padded", "insertion",
+                                                             "decode_gqa", "decode_gqa_kv4", "decode_mqa", "mixed_gqa",
+                                                             "mixed_padded", "insertion",
                                                              "insertion_padded"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -24,7 +24,7 @@ VALUES_SRC = os.path.join(PKG, "hostgen", "token_values.c")
 VALUES_LIB = os.path.join(PKG, "libcb_values.so")
 
 CUDA_SOURCES = ["runtime.cu", "append_kv.cu", "plan.cu", "split_kv.cu", "prefill_tc.cu", "attention.cu",
-                "synth.cu", "decode_noalloc.cu", "selftest.cu"]
+                "synth.cu", "decode_noalloc.cu", "selftest.cu", "decode_tc.cu"]
 CXX_SOURCES = ["scheduler.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O3",

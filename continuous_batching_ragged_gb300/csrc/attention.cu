@@ -166,7 +166,7 @@ cb_status attention(const char* who, const void* q, int32_t num_q_heads, const c
   plan.dec_ctas = cb::decode_persistent_ctas(a);
   plan.dec_groups = a.num_heads / cb::decode_group_heads(a);
   plan.kv_bytes_per_key = 2 * a.num_kv_heads * a.head_dim * 2;
-  plan.dec_bytes_per_us_per_sm = cb::decode_rate_per_sm(cb::decode_group_heads(a));
+  plan.dec_bytes_per_us_per_sm = cb::decode_rate_for(a);
   plan.split_sms = 1;
   st = cb::launch_plan(a, plan, main);
   if (st != CB_OK) return st;
@@ -248,7 +248,7 @@ cb_status plan_step(const char* who, const cb_kv_cache* cache, int32_t num_q_hea
   rec.plan.dec_ctas = cb::decode_persistent_ctas(a);
   rec.plan.dec_groups = a.num_heads / cb::decode_group_heads(a);
   rec.plan.kv_bytes_per_key = 2 * a.num_kv_heads * a.head_dim * 2;
-  rec.plan.dec_bytes_per_us_per_sm = cb::decode_rate_per_sm(cb::decode_group_heads(a));
+  rec.plan.dec_bytes_per_us_per_sm = cb::decode_rate_for(a);
   st = cb::launch_plan(a, rec.plan, static_cast<cudaStream_t>(stream));
   if (st != CB_OK) return st;
   rec.cu = cu_seqlens_q;

@@ -31,6 +31,7 @@ enum : unsigned {
   kSitePfS = 1u << 19,           // prefill softmax: S ready
   kSitePfO = 1u << 20,           // prefill softmax: P V done
   kSiteSelfTest = 1u << 21,
+  kSiteDecodeTc = 1u << 22,      // with a prefill site bit: the same wait in the grouped tensor-core decode
 };
 
 constexpr float kLog2e = 1.4426950408889634f;

@@ -108,6 +108,8 @@ cb_status launch_plan(const AttnArgs& a, const StepPlan& plan, cudaStream_t stre
 // the query heads each of its units covers.
 int decode_persistent_ctas(const AttnArgs& a);
 int decode_group_heads(const AttnArgs& a);
+// Decode K/V bytes one SM streams per microsecond on the path `a` takes.
+float decode_rate_for(const AttnArgs& a);
 
 // Persistent decode over the plan's decode items (bf16, head_dim 128, block
 // size a multiple of 16).  `after_previous`: a programmatic dependent launch
@@ -125,6 +127,17 @@ size_t split_kv_workspace_bytes(bool row_mode, int32_t num_seqs, int32_t num_tok
                                 int32_t num_heads, int32_t head_dim, int32_t max_context_len);
 cb_status launch_split_kv(const AttnArgs& a, bool row_mode, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream);
+
+// Decode rows with grouped key/value heads (4 < G <= 32 query heads per
+// key/value head, bf16, head_dim 128, power-of-two block size in [16, 128])
+// on tcgen05 tensor cores: persistent, one CTA per SM, one unit per
+// (decode item, key/value head).  decode_tc_ctas sets the kernel's shared
+// memory limit once per device and returns its grid size (0 on error).
+bool decode_tc_applies(const AttnArgs& a);
+float decode_tc_rate_per_sm(int group_heads);
+int decode_tc_ctas();
+cb_status launch_decode_tc(const AttnArgs& a, const StepPlan& plan, bool after_previous, bool wait_previous,
+                           cudaStream_t stream);
 
 // Prefill chunks (q_len > 1) on tcgen05 tensor cores, bf16, head_dim 128:
 // persistent CTAs over the plan's prefill items.

@@ -747,13 +747,20 @@ static void launch(const SplitArgs& sa, dim3 grid, cudaStream_t stream) {
   split_kv_kernel<T, A, ROW><<<grid, kWarps * 32, 0, stream>>>(sa);
 }
 
-// Query heads per decode unit: the largest of 4, 3, 2, 1 dividing the query
-// heads per KV head (1 for multi-head attention).
+// Query heads per decode unit: all G query heads of a key/value head on the
+// tensor-core path; otherwise the largest of 4, 3, 2, 1 dividing G (1 for
+// multi-head attention).
 int decode_group_heads(const AttnArgs& a) {
   const int G = a.num_kv_heads > 0 ? a.num_heads / a.num_kv_heads : 1;
+  if (decode_tc_applies(a)) return G;
   for (int gu = 4; gu > 1; --gu)
     if (G % gu == 0) return gu;
   return 1;
+}
+
+float decode_rate_for(const AttnArgs& a) {
+  if (decode_tc_applies(a)) return decode_tc_rate_per_sm(decode_group_heads(a));
+  return decode_rate_per_sm(decode_group_heads(a));
 }
 
 float decode_rate_per_sm(int group_heads) {
@@ -790,6 +797,7 @@ static int persistent_ctas(int dev) {
 }
 
 int decode_persistent_ctas(const AttnArgs& a) {
+  if (decode_tc_applies(a)) return decode_tc_ctas();
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     fail(CB_ERR_UNSUPPORTED, "decode: no usable current device");
@@ -810,6 +818,7 @@ static bool persistent_ok(const AttnArgs& a) {
 cb_status launch_decode_persistent(const AttnArgs& a, const StepPlan& plan, bool after_plan,
                                    bool wait_previous, cudaStream_t stream) {
   NvtxRange nvtx("cb.decode");
+  if (decode_tc_applies(a)) return launch_decode_tc(a, plan, after_plan, wait_previous, stream);
   SplitArgs sa;
   sa.wait_previous = wait_previous ? 1 : 0;
   sa.a = a;
@@ -879,7 +888,7 @@ cb_status launch_split_kv(const AttnArgs& a, bool row_mode, void* workspace,
     plan.dec_ctas = decode_persistent_ctas(a);
     plan.dec_groups = a.num_heads / decode_group_heads(a);
     plan.kv_bytes_per_key = 2 * a.num_kv_heads * a.head_dim * (a.dtype == CB_DTYPE_BF16 ? 2 : 4);
-    plan.dec_bytes_per_us_per_sm = decode_rate_per_sm(decode_group_heads(a));
+    plan.dec_bytes_per_us_per_sm = decode_rate_for(a);
     st = launch_plan(a, plan, stream);
     if (st != CB_OK) return st;
     return launch_decode_persistent(a, plan, true, true, stream);

@@ -1,8 +1,8 @@
 """Grouped-query attention (fewer key/value heads than query heads; not on the
 pages): query head h attends with key/value head h // (H / H_kv).  Decode rows
-(units of up to four query heads sharing one K/V stream), prefill chunks and
-mixed steps against the oracle, for groups of 2, 3, 4 and 8 heads and for one
-key/value head (MQA)."""
+(all query heads of a key/value head as the rows of one tensor-core unit),
+prefill chunks and mixed steps against the oracle, for groups of 2 to 32
+heads and for one key/value head (MQA)."""
 import numpy as np
 import pytest
 import torch
@@ -26,20 +26,45 @@ def test_gqa_decode_prefill_and_mixed(native_lib, H, Hkv):
     assert_tolerance(got, oracle_packed(b))
 
 
-def test_gqa_decode_full_size_sampled(native_lib):
-    """The decode workload with 32 query and 8 key/value heads: 256 sequences,
-    contexts 512-4096; sampled (sequence, head) rows against the oracle."""
+@pytest.mark.parametrize("Hkv", [8, 4, 1])
+def test_gqa_decode_full_size_every_row(native_lib, Hkv):
+    """The decode workload with 32 query heads over 8, 4 and 1 key/value heads
+    (groups of 4 on the CUDA-core path; 8 and 32 on the tensor-core path): 256
+    sequences, contexts 512-4096; every sequence on 4 query heads against the
+    oracle."""
     from gpu_harness import DeviceStep, assert_tolerance, oracle_rows, to_np
-    b = W.decode_step(num_kv_heads=8)
+    b = W.decode_step(num_kv_heads=Hkv)
     st = DeviceStep(b, source="device")
     out = to_np(st.run())
+    assert np.all(np.isfinite(out))
     rng = np.random.default_rng(3)
     got, exp = [], []
-    for s in rng.choice(b.num_seqs, 12, replace=False):
+    for s in range(b.num_seqs):
         heads = sorted(rng.choice(32, 4, replace=False).tolist())
-        exp.append(oracle_rows(b, int(s), heads)[0])
+        exp.append(oracle_rows(b, s, heads)[0])
         got.append(out[int(b.cu_seqlens_q[s])][heads])
     assert_tolerance(np.stack(got), np.stack(exp))
+
+
+@pytest.mark.parametrize("H,Hkv,B", [(64, 2, 16), (16, 2, 32), (40, 8, 64), (16, 1, 128), (96, 4, 16),
+                                     (4, 2, 32), (16, 4, 64)])
+def test_gqa_decode_groups_and_block_sizes(native_lib, H, Hkv, B):
+    """Grouped decode rows: groups of 5 to 32 query heads (the tensor-core
+    path; 32 fills its softmax warp) and of 2 and 4 (the CUDA-core path), every
+    block size, contexts around the 128-key tile, the 512-key split and block
+    edges, up to 9 splits per row; twice in a row, so the split tickets are
+    back at zero between calls."""
+    from gpu_harness import DeviceStep, assert_tolerance, oracle_packed, to_np
+    ctx = [1, 2, 127, 128, 129, 511, 512, 513, 1025, 2300, 4097]
+    b = W.make_batch([c - 1 for c in ctx], [1] * len(ctx), num_heads=H, head_dim=128, block_size=B,
+                     dtype="bf16", seed=300 + H + B, num_kv_heads=Hkv)
+    st = DeviceStep(b)
+    exp = oracle_packed(b)
+    first = st.run().clone()
+    assert_tolerance(to_np(first), exp)
+    st.attend()
+    torch.cuda.synchronize()
+    assert torch.equal(st.out.view(torch.int16), first.view(torch.int16))
 
 
 def test_gqa_head_groups_do_not_leak(native_lib):

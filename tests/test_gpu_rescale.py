@@ -95,11 +95,13 @@ def test_prefill_segments_rescale_forced(native_lib, kv_heads):
     assert_tolerance(got, oracle_packed(b))
 
 
-@pytest.mark.parametrize("heads,kv_heads", [(8, 2), (8, 4), (12, 4), (8, 8)])
+@pytest.mark.parametrize("heads,kv_heads", [(8, 2), (8, 4), (12, 4), (8, 8), (16, 2), (32, 1)])
 def test_decode_rescale_forced(native_lib, heads, kv_heads):
-    """Decode rows: the grouped kernel (4, 2 or 3 query heads per unit) keeps a
-    lazy maximum per warp; the one-head kernel rescales every tile.  Contexts
-    from one tile to 4000 keys, several splits per row."""
+    """Decode rows: the grouped CUDA-core kernel (4, 2 or 3 query heads per
+    unit) keeps a lazy maximum per warp; the one-head kernel rescales every
+    tile; the tensor-core kernel (groups of 8 and 32) keeps a lazy maximum per
+    row over 128-key tiles.  Contexts from one tile to 4000 keys, several
+    splits per row."""
     from gpu_harness import DeviceStep, assert_tolerance, oracle_packed, to_np
     ctx = [17, 33, 100, 800, 1500, 2500, 4000]
     b = W.make_batch([c - 1 for c in ctx], [1] * len(ctx), num_heads=heads, head_dim=128, block_size=16,
