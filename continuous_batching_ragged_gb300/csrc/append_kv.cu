@@ -100,7 +100,7 @@ cb_status append(const void* k_new, const void* v_new, const int64_t* slot_mappi
   // one CTA per token; with device sizes the step may be far below the
   // capacity, so a few CTAs per SM stride over whatever the step holds
   int64_t grid = num_tokens;
-  if (dims) grid = std::min<int64_t>(grid, int64_t(cb::sm_count()) * 8);
+  if (dims) grid = std::min<int64_t>(grid, int64_t(cb::sm_count()) * 2);
   append_kv_kernel<<<unsigned(grid), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
       static_cast<uint4*>(cache->k), static_cast<uint4*>(cache->v), num_tokens, heads_x_chunks,

@@ -298,10 +298,12 @@ cb_status attention_planned(const char* who, const void* q, int32_t num_q_heads,
     return cb::fail(CB_ERR_INVALID, "%s: the workspace's plan was made for other metadata, sizes or cache shape",
                     who);
   cudaStream_t main = static_cast<cudaStream_t>(stream);
-  // the claim counters start at zero for every call over the plan
-  cudaError_t e = cudaMemsetAsync(rec.plan.header + 2, 0, 2 * sizeof(int32_t), main);
-  if (e != cudaSuccess) return cb::cuda_fail(e, "clearing the claim counters");
-  return run_both(a, rec.plan, false, main);
+  // The claim counters are back at zero: the plan zeroes them and every
+  // persistent grid's last CTA resets its own.  The prefill kernel goes out
+  // as a programmatic dependent of whatever kernel precedes it (the layer's
+  // append): it waits for that grid on the device before reading anything,
+  // so only its launch overlaps.
+  return run_both(a, rec.plan, true, main);
 }
 
 }  // namespace

@@ -121,6 +121,7 @@ struct DecodeTcWork {
   const int2* items;        // the plan's decode items (sequence, split), longest first
   const int32_t* header;    // [0] items, [4] call tag, [5] keys per split
   int32_t* claims;          // unit claim counter
+  int32_t* done;            // CTAs done claiming (the last resets both)
   int32_t* tickets;         // [num_seqs][kv heads] split arrival counters (zero between calls)
   float* partials;          // [num_seqs][H][max_splits][HD + 2] split results (acc, max, sum)
   int32_t item_cap;
@@ -335,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       kc += it.nt;
     }
     if (!ok && lane == 0) raise_error(a.err, kErrTimeout | kSiteDecodeTc | site);
+    if (lane == 0) release_claims(w.claims, w.done, min(int(gridDim.x), n_units));
     if (lane == 0) {
       // (error path) let copies still in flight land before the CTA exits
       for (uint32_t gk = kc > uint32_t(kKStages) ? kc - kKStages : 0; gk < kc; ++gk)
@@ -774,6 +776,7 @@ cb_status launch_decode_tc(const AttnArgs& a, const StepPlan& plan, bool after_p
   w.items = plan.dec_items;
   w.header = plan.header;
   w.claims = plan.header + 2;
+  w.done = plan.header + 11;
   w.tickets = plan.tickets;
   w.partials = plan.partials;
   w.item_cap = plan.dec_cap;

@@ -40,6 +40,18 @@ __device__ __forceinline__ void raise_error(unsigned* word, unsigned bits) {
   atomicOr(word, bits);
 }
 
+// A persistent grid's claim counter returns to zero for the next launch over
+// the same plan (the layers of a planned step): each CTA that claimed counts
+// itself in `done` once it will claim no more, and the last of the
+// `claimers` zeroes both.  The next launch reads them only after this grid
+// has completed.
+__device__ __forceinline__ void release_claims(int32_t* claims, int32_t* done, int claimers) {
+  if (atomicAdd(done, 1) == claimers - 1) {
+    atomicExch(claims, 0);
+    atomicExch(done, 0);
+  }
+}
+
 // 2^x on the special function unit (PTX ex2.approx; ex2(-inf) = +0).
 __device__ __forceinline__ float ex2(float x) {
   float y;

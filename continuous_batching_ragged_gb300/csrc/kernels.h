@@ -62,7 +62,9 @@ struct StepPlan {
   int32_t* header;        // [0] decode items, [1] prefill units, [2] decode claims, [3] prefill claims,
                           // [4] call tag, [5] keys per decode split, [6] num_seqs, [7] num_tokens,
                           // [8] prefill CTAs that work (the rest leave their SMs to decode),
-                          // [9] KV tiles per prefill segment (0: units are not segmented)
+                          // [9] KV tiles per prefill segment (0: units are not segmented),
+                          // [10] / [11] prefill / decode CTAs done claiming (the last resets
+                          // its claim counter, so every launch over a plan starts at zero)
   int2* dec_items;        // (sequence, split) of every q_len == 1 row, longest first
   int2* dec_scratch;      // the decode items before sorting
   int2* pre_seqs;         // (sequence, query pairs) of every q_len > 1 chunk, costliest chunk first

@@ -420,6 +420,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
     p.header[7] = z.num_tokens;
     p.header[8] = k;
     p.header[9] = seg;
+    p.header[10] = 0;                     // prefill CTAs done claiming
+    p.header[11] = 0;                     // decode CTAs done claiming
   }
 }
 

@@ -315,6 +315,7 @@ struct PrefillWork {
   float* partials;          // [slot][HD + 2][256 rows] segment results (acc, max, sum), dimension-major
   const int32_t* header;    // [1] = number of units
   int32_t* claims;          // claim counter
+  int32_t* done;            // CTAs done claiming (the last resets both)
   int32_t unit_cap;         // capacity of the unit list
   uint32_t tag;             // the plan's call tag
 };
@@ -510,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       kc += sh.n;
     }
     if (!ok && lane == 0) raise_error(a.err, kErrTimeout | site);
+    if (lane == 0) release_claims(w.claims, w.done, min(int(gridDim.x), min(n_units, working)));
     if (lane == 0) {
       // (error path) let copies still in flight land before the CTA exits
       for (uint32_t g = kc > uint32_t(kKStages) ? kc - kKStages : 0; g < kc; ++g)
@@ -899,6 +901,7 @@ cb_status launch_prefill_tc(const AttnArgs& a, const StepPlan& plan, bool after_
   w.partials = plan.pre_partials;
   w.header = plan.header;
   w.claims = plan.header + 3;
+  w.done = plan.header + 10;
   w.unit_cap = plan.pre_cap * a.num_heads + kPrefillSegSlots;
   w.tag = plan.tag;
   // one CTA per SM, never more than entries could exist

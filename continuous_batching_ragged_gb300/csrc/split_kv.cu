@@ -48,6 +48,7 @@ struct SplitArgs {
   const int2* items;        // persistent decode: the plan's (sequence, split) items
   const int32_t* header;    // persistent decode: [0] = number of items
   int32_t* claims;          // persistent decode: claim counter
+  int32_t* done;            // persistent decode: CTAs done claiming (the last resets both)
   int32_t item_cap;         // persistent decode: capacity of the item list
   uint32_t tag;             // persistent decode: the plan's call tag
   int32_t n_groups;         // persistent decode: units per item (query-head groups)
@@ -726,6 +727,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) split_kv_persistent_kernel(con
     sm100::mbar_wait(sm100::smem_u32(&bars[consumed % kStages]), (consumed / kStages) & 1);
     ++consumed;
   }
+  __syncthreads();                          // every claim of this CTA has returned
+  if (threadIdx.x == 0) release_claims(sa.claims, sa.done, min(int(gridDim.x), n_units));
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -828,6 +831,7 @@ cb_status launch_decode_persistent(const AttnArgs& a, const StepPlan& plan, bool
   sa.items = plan.dec_items;
   sa.header = plan.header;
   sa.claims = plan.header + 2;
+  sa.done = plan.header + 11;
   sa.item_cap = plan.dec_cap;
   sa.tag = plan.tag;
   if (!persistent_ok(a)) {
