@@ -663,11 +663,14 @@ def dominant_roofline(b, work, attn_ms, peaks):
     t_dec = work["decode_bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_pre = work["prefill_flops"] / (peaks["bf16_tflops"] * 1e12)
     if t_dec >= t_pre:
-        dom = {"kernel": "split_kv_persistent_kernel (decode rows)" if b.dtype == "bf16" else "split_kv_kernel",
+        group = b.num_heads // b.kv_heads
+        tensor_decode = b.dtype == "bf16" and 4 < group <= 32      # groups of more than four heads
+        dom = {"kernel": ("decode_tc_kernel (grouped decode rows on tensor cores)" if tensor_decode else
+                          "split_kv_persistent_kernel (decode rows)" if b.dtype == "bf16" else "split_kv_kernel"),
                "bound": "hbm", "achieved": work["decode_bytes"] / (attn_ms * 1e-3) / 1e9,
                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-        prof = ("split_kv_persistent_gqa_decode_64seq.md" if b.kv_heads != b.num_heads
-                else "split_kv_persistent_decode_64seq.md")
+        prof = ("decode_tc_mqa_64seq.md" if tensor_decode else
+                "split_kv_persistent_gqa_decode_64seq.md" if group > 1 else "split_kv_persistent_decode_64seq.md")
         alg = work["decode_bytes"]
     else:
         dom = {"kernel": "prefill_tc_kernel (prefill chunks)", "bound": "tensor",
