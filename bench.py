@@ -249,7 +249,7 @@ def _random_inputs(n_max, c_max, H, A, Hkv=None):
     return _RANDOM_CACHE[key]
 
 
-def time_oracle(b, budget_s: float, detail: bool = False):
+def time_oracle(b, budget_s: float, detail: bool = False, repeat: bool = False):
     """Time the oracle (as it stands) on a bounded sample of the workload's
     sequences, with random inputs of the workload's shapes (drawn once and
     sliced per sequence; drawing them is not timed).  Returns (tokens/s,
@@ -260,19 +260,26 @@ def time_oracle(b, budget_s: float, detail: bool = False):
     scale = 1.0 / math.sqrt(A)
     qbuf, kbuf, vbuf = _random_inputs(b.max_q_len, b.max_context_len, H, A, b.kv_heads)
     order = np.argsort(-b.q_len, kind="stable")          # prefill chunks first, then decodes
-    done_tokens, done_seqs, spent = 0, 0, 0.0
-    for s in order:
-        n, c = int(b.q_len[s]), int(b.context_lens[s])
-        t0 = time.perf_counter()
-        oa.attend_sequence(qbuf[:n], kbuf[:c], vbuf[:c], c - n, scale)
-        spent += time.perf_counter() - t0
-        done_tokens += n
-        done_seqs += 1
-        if spent >= budget_s:
+    done_tokens, done_seqs, spent, passes = 0, 0, 0.0, 0
+    while True:                                         # repeat: whole passes until the budget is spent
+        for s in order:
+            n, c = int(b.q_len[s]), int(b.context_lens[s])
+            t0 = time.perf_counter()
+            oa.attend_sequence(qbuf[:n], kbuf[:c], vbuf[:c], c - n, scale)
+            spent += time.perf_counter() - t0
+            done_tokens += n
+            done_seqs += 1
+            if spent >= budget_s:
+                break
+        passes += 1
+        if not repeat or spent >= budget_s:
             break
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     sample = (f"{done_seqs} of {b.num_seqs} sequences ({done_tokens} of {b.T} query tokens, all "
               f"{H} heads), fp64 numpy, random inputs of the workload's shapes")
+    if passes > 1:
+        sample = (f"{passes} passes over all {b.num_seqs} sequences ({done_tokens} query tokens, all {H} heads), "
+                  "fp64 numpy, random inputs of the workload's shapes")
     if detail:
         return done_tokens / spent, sample, cores, spent, done_tokens, done_seqs
     return done_tokens / spent, sample, cores, spent
@@ -803,7 +810,7 @@ def oracle_one_thread(workload, decode_seqs, budget):
     thread count of numpy's BLAS is fixed when it loads)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     code = ("import json, bench; b, _ = bench.make_workload(%r, %d); "
-            "tps, sample, cores, spent = bench.time_oracle(b, %f); "
+            "tps, sample, cores, spent = bench.time_oracle(b, %f, repeat=True); "
             "print(json.dumps([tps, sample]))" % (workload, decode_seqs, budget))
     try:
         r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
@@ -894,6 +901,11 @@ def measure_per_config(torch, api, W, peaks, args):
                                  min_seconds=0.5)
         del st
         torch.cuda.empty_cache()
+        if name == "tiny" and not args.no_cpu_baseline:
+            # the tiny step is the oracle's own scale: time it on all host cores and on one
+            tps, sample, cores, _ = time_oracle(b, 2.0, repeat=True)
+            res["cpu_baseline"] = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+            res["cpu_baseline_1thread"] = oracle_one_thread("tiny", 256, 2.0)
         out[label] = res
     res = measure_long_prompt(torch, api, W, peaks, max(5, min(args.steps, 30)), warm)
     out[res["config"]["workload"]] = res
