@@ -59,7 +59,7 @@ constexpr int HD = 128;                          // head dim
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr int kThreads = 128;
-constexpr int kWarpSm = 0, kWarpK = 1, kWarpV = 2, kWarpMma = 3;
+constexpr int kWarpK = 1, kWarpV = 2, kWarpMma = 3;   // warp 0: softmax and epilogue
 constexpr int kMaxGroup = 32;                    // query heads per key/value head: one softmax warp
 constexpr uint32_t kHalf = BM * 64 * 2;          // one 64-dim swizzled half of a tile: 16 KB
 constexpr uint32_t kTile = 2 * kHalf;            // 32 KB
@@ -160,12 +160,6 @@ __device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap* tm
     tma_load_3d(dst + bi * B * 128, tm, bar, 0, 0, zs[bi]);
     tma_load_3d(dst + kHalf + bi * B * 128, tm, bar, 64, 0, zs[bi]);
   }
-}
-
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)

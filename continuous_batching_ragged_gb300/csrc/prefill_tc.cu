@@ -732,10 +732,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < BN; ++c)
             if (kb + c > limit) sr[c] = __float_as_uint(-INFINITY);
         }
-        if (PADDED && kb < pad_k0 + pad_n && kb + BN > pad_k0) {   // the tile holds pad keys: mask them
+        if constexpr (PADDED) {
+          if (kb < pad_k0 + pad_n && kb + BN > pad_k0) {   // the tile holds pad keys: mask them
 #pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (unsigned(kb + c - pad_k0) < unsigned(pad_n)) sr[c] = __float_as_uint(-INFINITY);
+            for (int c = 0; c < BN; ++c)
+              if (unsigned(kb + c - pad_k0) < unsigned(pad_n)) sr[c] = __float_as_uint(-INFINITY);
+          }
         }
         {                                          // four independent max chains (latency, not issue, bound)
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
