@@ -29,6 +29,7 @@ namespace {
 constexpr int kPlanThreads = 256;
 constexpr int kCostBuckets = 4096;     // costs at or above the last bucket share it
 constexpr int kUnitsPerCta = 6;        // decode units per persistent CTA the split size aims for
+constexpr int kUnitsPerCtaDecodeOnly = 2;   // the same when no prefill chunk shares the step
 constexpr int kRowCache = 2048;        // rows whose (q_len, ctx) stay in shared memory after pass 1
 // Cost model of a mixed step's SM split, fitted on GB300 to the long-prompt
 // chunk and to %globaltimer stamps of the mixed step's two kernels running
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
 
   // Pass 1: check every row; total keys of the decode rows.
   uint64_t dec_keys = 0;
+  int any_prefill = 0;
   for (int s = tid; s < z.num_seqs; s += kPlanThreads) {
     const RowInfo r = row_info(a, z, s);
     if (s < kRowCache) row_cache[s] = make_int2(r.bad ? 0 : r.q_len, r.ctx);
@@ -207,14 +209,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
       raise_error(a.err, kErrInvalid);
     else if (r.q_len == 1)
       dec_keys += uint64_t(r.ctx);
+    else
+      any_prefill = 1;
   }
+  const bool decode_only = __syncthreads_or(any_prefill) == 0;
   uint64_t total_keys;
   block_excl_scan(dec_keys, warp_sums, total_keys);
   // Keys per decode split: every split pays a fixed cost (its merge and a
   // partial result round trip), so splits are as long as possible while the
   // decode grid still gets kUnitsPerCta units per CTA to balance over (a
-  // decode item is dec_groups units, one per group of query heads).
-  const uint64_t target = uint64_t(p.dec_ctas > 0 ? p.dec_ctas : 1) * kUnitsPerCta;
+  // decode item is dec_groups units, one per group of query heads).  A
+  // decode-only step has the whole GPU and no prefill to finish beside it,
+  // so fewer, longer units balance well enough: measured on GB300 (256
+  // rows, contexts 512-4096) 0.446 against 0.472 ms at 32/8 heads, 0.250
+  // against 0.292 at 32/4 and 0.123 against 0.142 at 32/1; beside prefill
+  // the longer units cost more than they save (mixed step at 32/8 heads
+  // 0.280 against 0.237 ms).
+  const uint64_t target =
+      uint64_t(p.dec_ctas > 0 ? p.dec_ctas : 1) * (decode_only ? kUnitsPerCtaDecodeOnly : kUnitsPerCta);
   const uint64_t groups = uint64_t(p.dec_groups > 0 ? p.dec_groups : a.num_heads);
   const uint64_t want = (total_keys * groups + target - 1) / target;
   const uint64_t per = want < uint64_t(kSplitKeys) ? uint64_t(kSplitKeys) : want;
