@@ -163,10 +163,7 @@ cb_status attention(const char* who, const void* q, int32_t num_q_heads, const c
   st = cb::step_plan_layout(workspace, workspace_bytes, num_seqs, num_tokens, a.num_heads, cache->head_dim,
                             max_context_len, &plan);
   if (st != CB_OK) return st;
-  plan.dec_ctas = cb::decode_persistent_ctas(a);
-  plan.dec_groups = a.num_heads / cb::decode_group_heads(a);
-  plan.kv_bytes_per_key = 2 * a.num_kv_heads * a.head_dim * 2;
-  plan.dec_bytes_per_us_per_sm = cb::decode_rate_for(a);
+  cb::set_decode_plan(a, &plan);
   plan.split_sms = 1;
   st = cb::launch_plan(a, plan, main);
   if (st != CB_OK) return st;
@@ -245,10 +242,7 @@ cb_status plan_step(const char* who, const cb_kv_cache* cache, int32_t num_q_hea
   st = cb::step_plan_layout(workspace, workspace_bytes, num_seqs, num_tokens, a.num_heads, cache->head_dim,
                             max_context_len, &rec.plan);
   if (st != CB_OK) return st;
-  rec.plan.dec_ctas = cb::decode_persistent_ctas(a);
-  rec.plan.dec_groups = a.num_heads / cb::decode_group_heads(a);
-  rec.plan.kv_bytes_per_key = 2 * a.num_kv_heads * a.head_dim * 2;
-  rec.plan.dec_bytes_per_us_per_sm = cb::decode_rate_for(a);
+  cb::set_decode_plan(a, &rec.plan);
   st = cb::launch_plan(a, rec.plan, static_cast<cudaStream_t>(stream));
   if (st != CB_OK) return st;
   rec.cu = cu_seqlens_q;

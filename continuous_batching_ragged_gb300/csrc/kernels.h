@@ -83,6 +83,8 @@ struct StepPlan {
   uint32_t tag;           // this call's tag: the plan writes it to header[4], the kernels check it
   int32_t dec_ctas;       // CTAs of the persistent decode grid (sets the split length)
   int32_t dec_groups;     // decode units per decode item (query-head groups)
+  float dec_units_per_cta[2];    // decode units per CTA the split length aims for: [0] in a
+                                 // decode-only step, [1] when prefill chunks share the step
   int32_t num_sms;        // SMs of the device (sets the prefill CTAs of a mixed step)
   int32_t kv_bytes_per_key;  // K and V bytes of one key over all key/value heads
   float dec_bytes_per_us_per_sm;  // decode K/V bytes one SM streams per microsecond
@@ -93,6 +95,9 @@ struct StepPlan {
 // `group_heads` query heads (measured on GB300: ~90 GB/s for one head, where
 // memory binds; ~32 GB/s for four, where the arithmetic does).
 float decode_rate_per_sm(int group_heads);
+// Fills the decode fields of a step plan (grid size, groups, units per CTA,
+// bytes per key and the decode rate of the SM-share model) for these args.
+void set_decode_plan(const AttnArgs& a, StepPlan* plan);
 
 // Workspace of a bf16 step (plan + split scratch) and its carving.
 size_t step_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_heads, int32_t head_dim,

@@ -28,8 +28,6 @@ namespace {
 
 constexpr int kPlanThreads = 256;
 constexpr int kCostBuckets = 4096;     // costs at or above the last bucket share it
-constexpr int kUnitsPerCta = 6;        // decode units per persistent CTA the split size aims for
-constexpr int kUnitsPerCtaDecodeOnly = 2;   // the same when no prefill chunk shares the step
 constexpr int kRowCache = 2048;        // rows whose (q_len, ctx) stay in shared memory after pass 1
 // Cost model of a mixed step's SM split, fitted on GB300 to the long-prompt
 // chunk and to %globaltimer stamps of the mixed step's two kernels running
@@ -215,19 +213,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
   const bool decode_only = __syncthreads_or(any_prefill) == 0;
   uint64_t total_keys;
   block_excl_scan(dec_keys, warp_sums, total_keys);
-  // Keys per decode split: every split pays a fixed cost (its merge and a
-  // partial result round trip), so splits are as long as possible while the
-  // decode grid still gets kUnitsPerCta units per CTA to balance over (a
-  // decode item is dec_groups units, one per group of query heads).  A
-  // decode-only step has the whole GPU and no prefill to finish beside it,
-  // so fewer, longer units balance well enough: measured on GB300 (256
-  // rows, contexts 512-4096) 0.446 against 0.472 ms at 32/8 heads, 0.250
-  // against 0.292 at 32/4 and 0.123 against 0.142 at 32/1; beside prefill
-  // the longer units cost more than they save (mixed step at 32/8 heads
-  // 0.280 against 0.237 ms).
-  const uint64_t target =
-      uint64_t(p.dec_ctas > 0 ? p.dec_ctas : 1) * (decode_only ? kUnitsPerCtaDecodeOnly : kUnitsPerCta);
+  // Keys per decode split: every split pays a fixed cost (its merge, a
+  // partial result written and read back, the pipeline fill of a new unit),
+  // so splits are as long as possible while a split stays within 1/u of a
+  // decode CTA's average share (total keys x groups of query heads / CTAs),
+  // u = dec_units_per_cta: greedy claiming, longest unit first, then ends
+  // every CTA within about one unit of the others.
   const uint64_t groups = uint64_t(p.dec_groups > 0 ? p.dec_groups : a.num_heads);
+  const float per_cta = fmaxf(p.dec_units_per_cta[decode_only ? 0 : 1], 0.125f);
+  const uint64_t target = uint64_t(ceilf(float(p.dec_ctas > 0 ? p.dec_ctas : 1) * per_cta));
   const uint64_t want = (total_keys * groups + target - 1) / target;
   const uint64_t per = want < uint64_t(kSplitKeys) ? uint64_t(kSplitKeys) : want;
   const uint64_t rounded = (per + kSplitKeys - 1) / kSplitKeys * kSplitKeys;

@@ -39,6 +39,12 @@ constexpr int kWarps = 4;
 constexpr int kTile = 16;     // keys per warp iteration
 constexpr int kStages = 3;    // bulk-copy ring depth per warp
 constexpr uint32_t kTileBytes = kTile * 128 * 2;   // one bf16 16 x 128 K (or V) tile: 4 KB
+// Decode units per persistent CTA that the step plan's split length aims
+// for, in a decode-only step [0] and beside prefill chunks [1], for this
+// kernel and for the tensor-core one, whose units pay more at each start
+// (the query rows, the first tiles and the merge of every split).
+constexpr float kUnitsPerCta[2] = {2.f, 6.f};
+constexpr float kTcUnitsPerCta[2] = {1.f, 1.f};
 
 struct SplitArgs {
   AttnArgs a;
@@ -799,6 +805,16 @@ static int persistent_ctas(int dev) {
   return ctas_per_sm[dev] * sm_count();
 }
 
+void set_decode_plan(const AttnArgs& a, StepPlan* plan) {
+  const bool tc = decode_tc_applies(a);
+  plan->dec_ctas = decode_persistent_ctas(a);
+  plan->dec_groups = a.num_heads / decode_group_heads(a);
+  plan->dec_units_per_cta[0] = tc ? kTcUnitsPerCta[0] : kUnitsPerCta[0];
+  plan->dec_units_per_cta[1] = tc ? kTcUnitsPerCta[1] : kUnitsPerCta[1];
+  plan->kv_bytes_per_key = 2 * a.num_kv_heads * a.head_dim * (a.dtype == CB_DTYPE_BF16 ? 2 : 4);
+  plan->dec_bytes_per_us_per_sm = decode_rate_for(a);
+}
+
 int decode_persistent_ctas(const AttnArgs& a) {
   if (decode_tc_applies(a)) return decode_tc_ctas();
   int dev = 0;
@@ -889,10 +905,7 @@ cb_status launch_split_kv(const AttnArgs& a, bool row_mode, void* workspace,
     cb_status st = step_plan_layout(workspace, workspace_bytes, a.num_seqs, a.num_tokens, a.num_heads,
                                     a.head_dim, a.max_context_len, &plan);
     if (st != CB_OK) return st;
-    plan.dec_ctas = decode_persistent_ctas(a);
-    plan.dec_groups = a.num_heads / decode_group_heads(a);
-    plan.kv_bytes_per_key = 2 * a.num_kv_heads * a.head_dim * (a.dtype == CB_DTYPE_BF16 ? 2 : 4);
-    plan.dec_bytes_per_us_per_sm = decode_rate_for(a);
+    set_decode_plan(a, &plan);
     st = launch_plan(a, plan, stream);
     if (st != CB_OK) return st;
     return launch_decode_persistent(a, plan, true, true, stream);
