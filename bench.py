@@ -863,7 +863,8 @@ def measure_long_prompt(torch, api, W, peaks, steps, warmup):
     clocks = sampler.stop()
     api.cb_check_device_errors()
     ms = t0.elapsed_time(t1) / steps
-    attn_ms = sum(statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for ev in evs) for i in range(16))
+    chunk_attn_ms = [statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for ev in evs) for i in range(16)]
+    attn_ms = sum(chunk_attn_ms)
     append_ms = sum(statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for ev in evs) for i in range(16))
     flops = sum(w["prefill_flops"] for w in works)
     bytes_ = sum(w["bytes"] for w in works)
@@ -885,7 +886,10 @@ def measure_long_prompt(torch, api, W, peaks, steps, warmup):
                          "peak_source": f"of {peaks['source']}"},
             "step_roofline": {"flops": flops, "bytes": bytes_, "roofline_ms": max(t_tc, t_hbm) * 1e3,
                               "measured_ms": ms, "frac": max(t_tc, t_hbm) * 1e3 / ms,
-                              "append_ms": append_ms, "attention_ms": attn_ms},
+                              "append_ms": append_ms, "attention_ms": attn_ms,
+                              "chunk_attention_ms": [round(x, 4) for x in chunk_attn_ms],
+                              "chunk_tensor_frac": [round(w["prefill_flops"] / (x * 1e-3) / 1e12 / peaks["bf16_tflops"], 3)
+                                                    for w, x in zip(works, chunk_attn_ms)]},
             "clocks": clocks, "gpu_launches": 16 * 3 * steps}
 
 
