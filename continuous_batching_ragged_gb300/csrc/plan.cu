@@ -380,11 +380,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
   //    the pairs of one head then stream the same K/V together, read once
   //    from HBM, which the decode beside them saturates;
   //  * costliest pair first over all heads, then the next pair, in a
-  //    prefill-only step: greedy claiming then takes the longest units
-  //    first and ends on short ones (measured on GB300: a 2048-token chunk
-  //    at p = 0 in 0.069 against 0.086 ms, the 32768-token prompt in 16
-  //    chunks 7.68 against 7.91 ms; the mixed step with 64 decode rows
-  //    0.439 against 0.420 ms in this order, hence the first one there).
+  //    prefill-only step where the units differ in size: greedy claiming
+  //    then takes the longest units first and ends on short ones (measured
+  //    on GB300: a 2048-token chunk at p = 0 in 0.069 against 0.086 ms, the
+  //    32768-token prompt in 16 chunks 7.68 against 7.91 ms; the mixed step
+  //    with 64 decode rows 0.439 against 0.420 ms in this order, hence the
+  //    first one there).
   const bool pair_major = n_dec == 0;
   for (int u = tid; u < n_pre_units; u += kPlanThreads) {
     int lo = 0, hi = n_chunks - 1;
@@ -396,8 +397,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
     const int2 r = row(rec.x);
     const int np = rec.y;
     const int local = u - p.pre_scratch[lo].x;
-    const int h = pair_major ? local % a.num_heads : local / np;
-    const int qp = pair_major ? np - 1 - local / a.num_heads : np - 1 - (local - h * np);
+    // pair-major only where unit sizes differ enough to matter (a causal
+    // chunk's first pairs are short): a head's pairs read the same keys, and
+    // head by head they do so together, once from HBM
+    const bool pm = pair_major && 2 * pair_tiles(r.x, r.y, 0) < pair_tiles(r.x, r.y, np - 1);
+    const int h = pm ? local % a.num_heads : local / np;
+    const int qp = pm ? np - 1 - local / a.num_heads : np - 1 - (local - h * np);
     const int nt = pair_tiles(r.x, r.y, qp);
     if (seg == 0) {
       p.pre_units[u] = make_int4(rec.x, qp | (h << 16), nt << 16, -1);
@@ -421,7 +426,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const AttnArgs 
       int cnt = 0;
       for (int q2 = 0; q2 < np; ++q2) cnt += pair_tiles(r.x, r.y, q2) > kk * seg ? 1 : 0;
       const int j0 = kk * seg, j1 = min(j0 + seg, nt);
-      const int pos = pair_major ? (np - 1 - qp) * a.num_heads + h : h * cnt + (np - 1 - qp);
+      // a group of whole segments keeps the head-by-head order; a group of
+      // last segments (sizes differ: its first pair is the shortest) may go
+      // pair-major
+      const bool pm_kk = pair_major && pair_tiles(r.x, r.y, np - cnt) < j0 + seg;
+      const int pos = pm_kk ? (np - 1 - qp) * a.num_heads + h : h * cnt + (np - 1 - qp);
       p.pre_units[e_c + off + pos] = make_int4(rec.x, qp | (h << 16), j0 | (j1 << 16), slot0);
       off += cnt * a.num_heads;
     }
