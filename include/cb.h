@@ -1,7 +1,7 @@
 /*
  * cb.h -- C ABI of the ragged continuous-batching attention step on one GPU.
  *
- * One step of continuous batching, as the surveyed pages define it:
+ * One step of continuous batching, as these pages define it:
  *
  *   - Hugging Face blog "Continuous batching from first principles", section
  *     "Continuous batching": sequences are concatenated without padding
