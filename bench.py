@@ -662,6 +662,11 @@ def run_trace_bench(args, graph=False, print_line=True):
     return line
 
 
+def _sm_count() -> int:
+    import torch
+    return torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+
+
 def dominant_roofline(b, work, attn_ms, peaks):
     """Roofline of the step's dominant kernel: the larger of the decode rows'
     HBM time and the prefill chunks' tensor time.  Both kernels run inside the
@@ -671,7 +676,11 @@ def dominant_roofline(b, work, attn_ms, peaks):
     t_pre = work["prefill_flops"] / (peaks["bf16_tflops"] * 1e12)
     if t_dec >= t_pre:
         group = b.num_heads // b.kv_heads
-        tensor_decode = b.dtype == "bf16" and 4 < group <= 32      # groups of more than four heads
+        # the library's routing: groups of 5..32 heads on tensor cores, groups
+        # of four too unless the step is decode-only with at least 8 units
+        # (sequence, key/value head) per SM
+        tensor_decode = b.dtype == "bf16" and (4 < group <= 32 or (group == 4 and (
+            b.max_q_len > 1 or b.num_seqs * b.kv_heads < 8 * _sm_count())))
         dom = {"kernel": ("decode_tc_kernel (grouped decode rows on tensor cores)" if tensor_decode else
                           "split_kv_persistent_kernel (decode rows)" if b.dtype == "bf16" else "split_kv_kernel"),
                "bound": "hbm", "achieved": work["decode_bytes"] / (attn_ms * 1e-3) / 1e9,

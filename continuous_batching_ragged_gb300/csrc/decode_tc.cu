@@ -61,6 +61,7 @@ constexpr int kVStages = 2;
 constexpr int kThreads = 128;
 constexpr int kWarpK = 1, kWarpV = 2, kWarpMma = 3;   // warp 0: softmax and epilogue
 constexpr int kMaxGroup = 32;                    // query heads per key/value head: one softmax warp
+constexpr int kG4CudaCoreUnitsPerSm = 8;         // groups of four go to CUDA cores from this many units per SM
 constexpr uint32_t kHalf = BM * 64 * 2;          // one 64-dim swizzled half of a tile: 16 KB
 constexpr uint32_t kTile = 2 * kHalf;            // 32 KB
 constexpr uint32_t kTmemCols = 512;              // S buffers at 0 and 128, O at 256
@@ -694,14 +695,23 @@ bool g_attr_set[64] = {};
 // Groups of more than four query heads: the CUDA-core kernel's units cover
 // at most four, so it would stream each K/V tile G/4 times (or G times for a
 // G with no divisor in 2..4); here every tile is streamed once for all G.
-// For G <= 4 the two read the same bytes and take the same time (0.47 ms on
-// the 256-sequence decode step at 32/8 heads), and the CUDA-core kernel's
-// rate model for mixed steps is the measured one, so it keeps those.
+// Groups of four read the same bytes in both kernels: the choice below is by
+// measured time.  Groups of two and three keep the CUDA-core kernel.
 bool decode_tc_applies(const AttnArgs& a) {
   const int G = a.num_kv_heads > 0 ? a.num_heads / a.num_kv_heads : 1;
   const int B = a.block_size;
-  return a.dtype == CB_DTYPE_BF16 && a.head_dim == HD && G > 4 && G <= kMaxGroup &&
-         a.num_heads == G * a.num_kv_heads && B >= 16 && B <= BN && (B & (B - 1)) == 0;
+  if (!(a.dtype == CB_DTYPE_BF16 && a.head_dim == HD && G >= 4 && G <= kMaxGroup &&
+        a.num_heads == G * a.num_kv_heads && B >= 16 && B <= BN && (B & (B - 1)) == 0))
+    return false;
+  if (G > 4) return true;
+  // Groups of four: the CUDA-core kernel is faster on large decode-only
+  // steps (256 rows at 32/8 heads: 0.448 against 0.473 ms on GB300), this
+  // one elsewhere (64 rows: 0.136 against 0.188 ms; the 2048-token mixed
+  // step: 0.217 against 0.239 ms; the 32-layer serving trace replayed as
+  // CUDA graphs: 4.06 against 4.67 ms per step).  Sizes that live on the
+  // device (graph replay) take this kernel.
+  return a.dims != nullptr || a.max_q_len > 1 ||
+         int64_t(a.num_seqs) * a.num_kv_heads < int64_t(kG4CudaCoreUnitsPerSm) * sm_count();
 }
 
 // K/V bytes one SM streams per microsecond (measured on GB300, 256-sequence
