@@ -686,7 +686,7 @@ def dominant_roofline(b, work, attn_ms, peaks):
                "bound": "hbm", "achieved": work["decode_bytes"] / (attn_ms * 1e-3) / 1e9,
                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
         prof = ("decode_tc_mqa_64seq.md" if tensor_decode else
-                "split_kv_persistent_gqa_decode_64seq.md" if group > 1 else "split_kv_persistent_decode_64seq.md")
+                "split_kv_persistent_gqa_decode_160seq.md" if group > 1 else "split_kv_persistent_decode_64seq.md")
         alg = work["decode_bytes"]
     else:
         dom = {"kernel": "prefill_tc_kernel (prefill chunks)", "bound": "tensor",
