@@ -12,18 +12,14 @@
 // A unit is (sequence, split, key/value head): the G query rows of one decode
 // token against keys [k0, k1) of one split (the step plan's decode items,
 // times the key/value heads).  The G rows occupy the first rows of a
-// 128-row A operand (tcgen05 MMAs have at least 64 rows).  Only 32 rows are
-// stored (rows G..31 zero); the descriptor's rows 32..127 fall on the
-// shared memory behind them, whatever it holds: those rows of S, P and O
-// live in TMEM lanes 32..127, which no thread reads, and MMA rows are
-// independent, so they cannot reach rows 0..G-1.  And a
+// 128-row tile (tcgen05 MMAs have at least 64 rows; the rest are zero), and a
 // KV tile is 128 keys of 128/B paged blocks, one 3-D TMA box per block and
 // 64-dim half, 128-byte swizzled -- the same boxes as the prefill kernel.
 //   * warp 1 (K loader) claims units, publishes them in a two-slot item ring,
 //     loads each unit's G query rows (once the previous unit's last S has
 //     read the tile) and streams K tiles into a 3-stage ring, looking the
 //     block table up four tiles ahead and prefetching those boxes into L2;
-//   * warp 2 (V loader) streams V tiles into a 3-stage ring and zeroes the
+//   * warp 2 (V loader) streams V tiles into a 2-stage ring and zeroes the
 //     rows past the context in the last paged block (P is 0 there, but
 //     0 * NaN is NaN);
 //   * warp 3 (MMA, one thread): S into two TMEM buffers in turn, so the
@@ -40,7 +36,7 @@
 //     normalised rows or, for a row cut into splits, its partial (acc, max,
 //     sum); the last split of a (sequence, key/value head) to finish merges
 //     every split by log-sum-exp.
-// One CTA per SM (about 200 KB of shared memory).  Every wait is bounded; a
+// One CTA per SM (about 193 KB of shared memory).  Every wait is bounded; a
 // timeout sets the device error word and the CTA winds down, freeing TMEM.
 #include <algorithm>
 #include <mutex>
@@ -61,19 +57,18 @@ constexpr int BM = 128;                          // MMA rows: the unit's G query
 constexpr int BN = 128;                          // keys per KV tile
 constexpr int HD = 128;                          // head dim
 constexpr int kKStages = 3;
-constexpr int kVStages = 3;                      // (K 3 / V 3 beat K 3 / V 2 and K 4 / V 2 by ~1 %)
+constexpr int kVStages = 2;
 constexpr int kThreads = 128;
 constexpr int kWarpK = 1, kWarpV = 2, kWarpMma = 3;   // warp 0: softmax and epilogue
 constexpr int kMaxGroup = 32;                    // query heads per key/value head: one softmax warp
-constexpr int kG4CudaCoreUnitsPerSm = 8;         // groups of four go to CUDA cores from this many units per SM
+constexpr int kG4CudaCoreUnitsPerSm = 10;        // groups of four go to CUDA cores from this many units per SM
 constexpr uint32_t kHalf = BM * 64 * 2;          // one 64-dim swizzled half of a tile: 16 KB
 constexpr uint32_t kTile = 2 * kHalf;            // 32 KB
 constexpr uint32_t kTmemCols = 512;              // S buffers at 0 and 128, O at 256
 constexpr uint32_t kColO = 256;
 
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kQHalf = kMaxGroup * 128;   // one 64-dim half of the query rows: 4 KB
-constexpr uint32_t kOffK = kOffQ + 2 * kQHalf;
+constexpr uint32_t kOffK = kOffQ + kTile;
 constexpr uint32_t kOffV = kOffK + kKStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
 constexpr int kItemSlots = 2;
@@ -195,8 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_units = n_items * Hkv;
   if (int(blockIdx.x) >= n_units) return;
 
-  // rows G..31 of the query rows stay zero for the whole launch
-  for (uint32_t o = threadIdx.x * 16; o < 2 * kQHalf; o += kThreads * 16)
+  // rows G..127 of the query tile stay zero for the whole launch
+  for (uint32_t o = threadIdx.x * 16; o < kTile; o += kThreads * 16)
     *reinterpret_cast<uint4*>(gsm + kOffQ + o) = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
@@ -299,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(BAR_Q), 2u * uint32_t(G) * 128u);
           tma_load_3d(base + kOffQ, &tm_q, bar(BAR_Q), 0, it.g * G, it.t);
-          tma_load_3d(base + kOffQ + kQHalf, &tm_q, bar(BAR_Q), 64, it.g * G, it.t);
+          tma_load_3d(base + kOffQ + kHalf, &tm_q, bar(BAR_Q), 64, it.g * G, it.t);
         }
         __syncwarp();
         return true;
@@ -419,8 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < HD / 16; ++k) {
         const uint32_t off16 = ((k / 4) * kHalf + (k % 4) * 32) >> 4;
-        const uint32_t qoff16 = ((k / 4) * kQHalf + (k % 4) * 32) >> 4;
-        mma_f16_ss(tmem + 128 * buf, dq + qoff16, kd + off16, idS, k > 0);
+        mma_f16_ss(tmem + 128 * buf, dq + off16, kd + off16, idS, k > 0);
       }
       mma_commit(bar(BAR_S + buf));
     };
@@ -711,11 +705,12 @@ bool decode_tc_applies(const AttnArgs& a) {
     return false;
   if (G > 4) return true;
   // Groups of four: the CUDA-core kernel is faster on large decode-only
-  // steps (256 rows at 32/8 heads: 0.448 against 0.473 ms on GB300), this
-  // one elsewhere (64 rows: 0.136 against 0.188 ms; the 2048-token mixed
-  // step: 0.217 against 0.239 ms; the 32-layer serving trace replayed as
-  // CUDA graphs: 4.06 against 4.67 ms per step).  Sizes that live on the
-  // device (graph replay) take this kernel.
+  // steps, this one elsewhere.  Measured on GB300 at 32/8 heads (CUDA cores
+  // against tensor cores): decode steps of 256 rows 0.446 / 0.469 ms, 200
+  // rows 0.378 / 0.378, 160 rows 0.330 / 0.315, 96 rows 0.249 / 0.196;
+  // the 2048-token mixed step 0.239 / 0.217; the 32-layer serving trace
+  // replayed as CUDA graphs 4.67 / 4.06 ms per step.  Sizes that live on
+  // the device (graph replay) take this kernel.
   return a.dims != nullptr || a.max_q_len > 1 ||
          int64_t(a.num_seqs) * a.num_kv_heads < int64_t(kG4CudaCoreUnitsPerSm) * sm_count();
 }

@@ -45,6 +45,7 @@ constexpr uint32_t kTileBytes = kTile * 128 * 2;   // one bf16 16 x 128 K (or V)
 // (the query rows, the first tiles and the merge of every split).
 constexpr float kUnitsPerCta[2] = {2.f, 6.f};
 constexpr float kTcUnitsPerCta[2] = {1.f, 1.f};
+constexpr float kTcUnitsPerCtaWide = 0.75f;   // groups of more than 16 heads (MQA at 32 heads)
 
 struct SplitArgs {
   AttnArgs a;
@@ -809,8 +810,9 @@ void set_decode_plan(const AttnArgs& a, StepPlan* plan) {
   const bool tc = decode_tc_applies(a);
   plan->dec_ctas = decode_persistent_ctas(a);
   plan->dec_groups = a.num_heads / decode_group_heads(a);
-  plan->dec_units_per_cta[0] = tc ? kTcUnitsPerCta[0] : kUnitsPerCta[0];
-  plan->dec_units_per_cta[1] = tc ? kTcUnitsPerCta[1] : kUnitsPerCta[1];
+  const bool wide = tc && decode_group_heads(a) > 16;
+  plan->dec_units_per_cta[0] = wide ? kTcUnitsPerCtaWide : tc ? kTcUnitsPerCta[0] : kUnitsPerCta[0];
+  plan->dec_units_per_cta[1] = wide ? kTcUnitsPerCtaWide : tc ? kTcUnitsPerCta[1] : kUnitsPerCta[1];
   plan->kv_bytes_per_key = 2 * a.num_kv_heads * a.head_dim * (a.dtype == CB_DTYPE_BF16 ? 2 : 4);
   plan->dec_bytes_per_us_per_sm = decode_rate_for(a);
 }
