@@ -677,16 +677,16 @@ def dominant_roofline(b, work, attn_ms, peaks):
     if t_dec >= t_pre:
         group = b.num_heads // b.kv_heads
         # the library's routing: groups of 5..32 heads on tensor cores, groups
-        # of four too unless the step is decode-only with at least 8 units
+        # of four too unless the step is decode-only with at least 10 units
         # (sequence, key/value head) per SM
         tensor_decode = b.dtype == "bf16" and (4 < group <= 32 or (group == 4 and (
-            b.max_q_len > 1 or b.num_seqs * b.kv_heads < 8 * _sm_count())))
+            b.max_q_len > 1 or b.num_seqs * b.kv_heads < 10 * _sm_count())))
         dom = {"kernel": ("decode_tc_kernel (grouped decode rows on tensor cores)" if tensor_decode else
                           "split_kv_persistent_kernel (decode rows)" if b.dtype == "bf16" else "split_kv_kernel"),
                "bound": "hbm", "achieved": work["decode_bytes"] / (attn_ms * 1e-3) / 1e9,
                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
         prof = ("decode_tc_mqa_64seq.md" if tensor_decode else
-                "split_kv_persistent_gqa_decode_160seq.md" if group > 1 else "split_kv_persistent_decode_64seq.md")
+                "split_kv_persistent_gqa_decode_200seq.md" if group > 1 else "split_kv_persistent_decode_64seq.md")
         alg = work["decode_bytes"]
     else:
         dom = {"kernel": "prefill_tc_kernel (prefill chunks)", "bound": "tensor",
