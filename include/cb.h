@@ -138,10 +138,18 @@ cb_status cb_ragged_attention(const void* q, const cb_kv_cache* cache,
  * multiple of H_kv, and query head h attends with key/value head
  * h / (num_q_heads / H_kv) (groups of consecutive query heads).  Otherwise
  * identical to cb_ragged_attention, which is the case num_q_heads = H_kv.
- * A decode unit covers up to four query heads of one group, so each K/V byte
- * read from memory serves all of them.  Grouped heads need bf16 and a block
- * size that is a multiple of 16 (CB_ERR_UNSUPPORTED otherwise); the workspace
- * must be cb_attention_workspace_size_gqa bytes.
+ * Decode rows of a group run on one of two kernels: CUDA cores, a unit
+ * covering up to four query heads of one group, or tensor cores (head_dim
+ * 128, groups of 4 to 32 heads), a unit covering the whole group; either way
+ * each K/V byte read from memory serves all the unit's heads.  Groups of more
+ * than four take the tensor cores; groups of four take them too except in
+ * decode-only steps with at least 10 (sequence, key/value head) units per SM
+ * given on the host (dims NULL).  The two kernels agree within fp32
+ * accumulation rounding, not bit for bit, so a step of groups of four can
+ * differ in its last bits between a host-sized call and a dims call.
+ * Grouped heads need bf16 and a block size that is a multiple of 16
+ * (CB_ERR_UNSUPPORTED otherwise); the workspace must be
+ * cb_attention_workspace_size_gqa bytes.
  * ------------------------------------------------------------------------- */
 size_t cb_attention_workspace_size_gqa(const cb_kv_cache* cache, int32_t num_q_heads,
                                        int32_t num_seqs, int32_t num_tokens, int32_t max_context_len);
